@@ -1,0 +1,283 @@
+"""Benchmark: Q4_K x q8 prefill GEMMs on GB300.
+
+Default workload: the 7B whole-prefill linear stack -- 32 layers x {q, k, v, o:
+4096x4096; gate, up: 11008x4096; down: 4096x11008} random Q4_K weights, 2048
+tokens, a distinct fp32 activation matrix per projection (224 buffers), fused
+q8 activation quantization, bf16 output.  One step = all 224 projections
+(activation quantization + GEMM each).  tok/s = 2048 / step time.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (no data
+exchange); value = all ranks' tokens / max step time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tok/s and effective INT8 TOPS (% of roofline), Q4_K×Q8 GEMM, 1×GB300"
+TOKENS = 2048
+LAYER = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
+         ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008)]
+
+WORKLOADS = {
+    # name: (tokens, [(n, k)] per step, out dtype, description)
+    "stack": (TOKENS, [(n, k) for _ in range(32) for (_, n, k) in LAYER], "bf16",
+              "7B whole-prefill linear stack: 32 layers x {q,k,v,o 4096x4096; gate,up 11008x4096; "
+              "down 4096x11008} Q4_K, 2048 tokens, fused q8 activation quantization, bf16 out"),
+    "ffn": (2048, [(11008, 4096), (11008, 4096), (4096, 11008)], "bf16",
+            "7B FFN linears gate/up 11008x4096 + down 4096x11008 Q4_K, 2048 tokens, fused q8, bf16 out"),
+    "qproj2630": (2630, [(4096, 4096)], "bf16", "7B q-proj 4096x4096 Q4_K, 2630 tokens (outlier channels), fused q8, bf16 out"),
+    "qproj512": (512, [(4096, 4096)], "f32", "7B q-proj 4096x4096 Q4_K, 512 tokens, fused q8, fp32 out"),
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)}
+
+
+def cpu_baseline(workload, seconds=10.0):
+    """The oracle as it stands, on a bounded sample: 32 tokens through one
+    q-proj-shaped matrix (4096x4096), repeated until `seconds` have passed;
+    the time is scaled to the workload by its total weight count."""
+    import numpy as np
+
+    from oracle import gemm as ogemm
+    from oracle import q4k_blocks, q8 as oq8
+    from quantized_prefill_gemm_gb300 import inputs
+
+    tokens, mats, _, _ = WORKLOADS[workload]
+    n, k, t = 4096, 4096, 32
+    fields = q4k_blocks.decode(inputs.q4k_blocks(n, k, 99))
+    x = inputs.activations(t, k, 99)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        qa, da, ss = oq8.quantize_rows(x)
+        ogemm.gemm_blockwise(fields, qa, da, ss)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    per = (time.perf_counter() - t0) / reps
+    scale = sum(nn * kk for nn, kk in mats) / (n * k)
+    step_s = per * scale * (tokens / t)
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": tokens / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{t} tokens x one 4096x4096 Q4_K matrix (numpy fp64 oracle: q8 quantization + blockwise "
+                      f"GEMM), {reps} repeats in {time.perf_counter() - t0:.1f} s, scaled by weight count "
+                      f"({scale:.1f}x) and tokens ({tokens // t}x) to the workload"}, step_s
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    base, step_s = cpu_baseline(args.workload, seconds=max(5.0, min(30.0, 3.0 * (args.steps + args.warmup))))
+    tokens, mats, _, desc = WORKLOADS[args.workload]
+    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats)},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+
+    from quantized_prefill_gemm_gb300 import inputs, q4k
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    tokens, mats, out, desc = WORKLOADS[args.workload]
+    kind = "outlier" if args.workload == "qproj2630" else "normal"
+    # weights (packed once, resident) and one activation matrix per projection
+    packed, xs, ys = [], [], []
+    for i, (n, k) in enumerate(mats):
+        blocks = inputs.q4k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
+        packed.append(q4k.q4k_pack_weights(blocks, n, k))
+        del blocks
+        kind_i = "silu_mul" if (args.workload == "ffn" and i == 2) else kind
+        xs.append(inputs.activations_torch(tokens, k, seed=4 + rank, kind=kind_i, tag=i, device=dev))
+        ys.append(torch.empty((tokens, n), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device=dev))
+    ws_bytes = max(q4k.q4k_act_workspace_bytes(tokens, k) for _, k in mats)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        for i, (n, k) in enumerate(mats):
+            q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
+            if events is not None:
+                events[i][0].record(stream)
+            q4k.q4k_gemm_quantized(packed[i], n, k, ws, tokens, out, y=ys[i], stream=stream)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in mats]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    ms_step = total_ms / args.steps
+    gemm_ms = sum(a.elapsed_time(b) for s in ev for (a, b) in s)
+    flops_step = sum(2.0 * tokens * n * k for n, k in mats)
+    err = q4k.q4k_device_error_word()
+    if err:
+        raise RuntimeError(f"device error word 0x{err:x}")
+
+    value = world * tokens / (ms_step * 1e-3)
+    eff_tops = world * flops_step / (ms_step * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops_step * args.steps / (gemm_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "q4k_gemm_kernel",
+                "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step); the GEMM issues "
+                               "f16 tcgen05 MMAs, same rate class",
+                "per_launch": "2*M*N*K algorithmic flops / CUDA-event duration of each GEMM launch"}
+
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
+
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers",
+            "data": "synthetic (seeded random Q4_K weights and activations)",
+            "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
+                       "l2": "inputs larger than L2 (whole step touches >18 GB)", "parallelism": f"replicas x{world}"},
+            "effective_tops": eff_tops, "gemm_ms_per_step": gemm_ms / args.steps,
+            "roofline": roofline, "clocks": clk, "gpu_launches": 2 * len(mats) * args.steps}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"], _ = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2):
+    """Same metric through the public fused call q4k_gemm, with every
+    projection's activations copied from pinned host memory and its result
+    copied back inside the timed region."""
+    host_x = [x.cpu().pin_memory() for x in xs]
+    ydt = torch.bfloat16 if out == "bf16" else torch.float32
+    host_y = [torch.empty((tokens, n), dtype=ydt, pin_memory=True) for n, _ in mats]
+    dx = {k: torch.empty((tokens, k), dtype=torch.float32, device=dev) for _, k in mats}
+    dy = {n: torch.empty((tokens, n), dtype=ydt, device=dev) for n, _ in mats}
+
+    def step():
+        for i, (n, k) in enumerate(mats):
+            dx[k].copy_(host_x[i], non_blocking=True)
+            q4k.q4k_gemm(packed[i], n, k, dx[k], out_dtype=out, y=dy[n], workspace=ws, stream=stream)
+            host_y[i].copy_(dy[n], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(tokens * k * 4 for _, k in mats)
+    d2h = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
+    return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

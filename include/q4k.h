@@ -1,0 +1,173 @@
+/*
+ * q4k.h -- C ABI of the Q4_K x q8 prefill GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (all page references are to the yusiwen.cn minfer
+ * "cuda_optimization_steps" pages):
+ *
+ *   Y[t, o] = sum_k W[o, k] * X[t, k]
+ *
+ * W is stored in Q4_K super-blocks (256 weights: f16 d and dmin, eight 32-weight
+ * sub-blocks with 6-bit scale sc and 6-bit min m, 4-bit quants q; w = d*sc*q -
+ * dmin*m).  X is quantized into 32-element q8 blocks, each with an f16 scale
+ * d_a and the i16 sum ssum of its q8 values ("34 · r31 — q-major sda
+ * scale-read repack", §1 Background).  Each 32-k chunk is reduced as an exact
+ * integer dot product and rescaled by the two-term rank-1 rescale
+ *   d_a*(d*sc)*sum(q*qa) + d_a*ssum*(-dmin*m)
+ * ("34 · r31", §1-§2: the A-side pair (d_a, ssum) and the B-side pair
+ * (d*sc, -dmin*m); "22 · r17 — Wide warp remap", §1: the r15 rank-1 fold).
+ *
+ * Conventions for every entry point
+ *   - Pointers named as device memory are device memory owned by the caller.
+ *     The library never allocates, frees or synchronises on these calls
+ *     (the diagnostics at the end of this header are the documented
+ *     exceptions: they synchronise).
+ *   - Every call is asynchronous on `stream` (0 = the legacy default stream).
+ *     The returned status covers argument validation and launch errors;
+ *     faults inside a kernel surface at the caller's next synchronisation.
+ *     Internal waits of the GEMM are bounded: on a timeout the kernel records
+ *     an error word (see q4k_device_status) and returns instead of hanging.
+ *   - Matrices are row-major; leading dimensions are in elements.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef Q4K_H
+#define Q4K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t;   /* same type as the CUDA runtime's */
+
+typedef enum q4k_status {
+    Q4K_OK = 0,
+    Q4K_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum  */
+    Q4K_ERR_SHAPE = 2,              /* k % 256, n % 128, ld < row length ...  */
+    Q4K_ERR_ALIGNMENT = 3,          /* pointer or leading dimension alignment */
+    Q4K_ERR_WORKSPACE = 4,          /* workspace / packed buffer too small    */
+    Q4K_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not sm_103           */
+    Q4K_ERR_CUDA = 6,               /* a CUDA runtime / driver call failed    */
+    Q4K_ERR_TIMEOUT = 7             /* a bounded device-side wait ran out     */
+} q4k_status;
+
+typedef enum q4k_act_kind {
+    Q4K_ACT_F32 = 0,   /* x is fp32 [m][ldx]; quantized inside q4k_gemm      */
+    Q4K_ACT_Q8 = 1     /* x is the q8 SoA of q8_quantize_rows (see there)    */
+} q4k_act_kind;
+
+typedef enum q4k_out_dtype {
+    Q4K_OUT_F32 = 0,
+    Q4K_OUT_BF16 = 1   /* fp32 result rounded to bf16, round-to-nearest-even */
+} q4k_out_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* q4k_status_string(int status);
+
+/* ABI version of this header (bumped on any incompatible change). */
+#define Q4K_ABI_VERSION 1
+int q4k_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * q8_quantize_rows -- activation quantization into 32-element q8 blocks.
+ * ("34 · r31 — q-major sda scale-read repack", §1: each q8 block carries an
+ * f16 scale d and an i16 ssum, the sum of its q8 values.)
+ * Per block of 32 consecutive k of one token:
+ *   amax = max|x|;  if amax < 2^-120: qa = 0, ssum = 0, d_a = +0;
+ *   else d = RN32(amax/127), inv = RN32(127/amax),
+ *        qa = clamp(rint_half_even(RN32(x*inv)), -127, 127),
+ *        ssum = sum(qa), d_a = RN16(d).
+ * Bit-exact by construction (IEEE fp32 ops in this order, no contraction).
+ *   x       device, fp32 [m][ldx]; 16-byte aligned, ldx % 4 == 0, ldx >= k
+ *   q8      device, int8 [m][k]   (4-byte aligned)
+ *   da_f16  device, f16 bit patterns [m][k/32]
+ *   ssum    device, int16 [m][k/32]
+ *   k % 32 == 0; m == 0 is a no-op.  x must be finite.
+ * ------------------------------------------------------------------------ */
+q4k_status q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx,
+                            int8_t* q8, uint16_t* da_f16, int16_t* ssum,
+                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Weight repack (load time, not on the per-token path).
+ * q4k_blocks  device, [n][k/256] canonical 144-byte Q4_K blocks (16-byte
+ *             aligned): bytes 0-1 d (f16), 2-3 dmin (f16), 4-15 the sixteen
+ *             6-bit scales/mins, 16-143 the 4-bit quants (GGUF Q4_K order).
+ * packed      device, q4k_packed_bytes(n, k) bytes (256-byte aligned); an
+ *             opaque layout consumed only by q4k_gemm / q4k_gemm_quantized.
+ * n % 128 == 0, k % 256 == 0.
+ * ------------------------------------------------------------------------ */
+size_t q4k_packed_bytes(int64_t n, int64_t k);
+q4k_status q4k_pack_weights(const void* q4k_blocks, int64_t n, int64_t k,
+                            void* packed, size_t packed_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * q4k_gemm -- Y = W * X^T with the per-32-k rescale (the path above).
+ *   packed_w  from q4k_pack_weights(n, k)
+ *   act == Q4K_ACT_F32: x_or_q8 = fp32 [m][ldx] (same rules as
+ *                       q8_quantize_rows); da_f16 and ssum are ignored.
+ *   act == Q4K_ACT_Q8 : x_or_q8 = int8 q8 [m][ldx] (ldx % 4 == 0, 4-byte
+ *                       aligned), da_f16 = f16 bits [m][k/32],
+ *                       ssum = int16 [m][k/32], as written by q8_quantize_rows.
+ *   y         device, [m][ldy] fp32 (ldy % 4 == 0) or bf16 (ldy % 8 == 0),
+ *             16-byte aligned; columns [n, ldy) are not touched.
+ *   workspace device, >= q4k_gemm_workspace_bytes(m, n, k, act) bytes,
+ *             256-byte aligned; contents are scratch, overwritten per call.
+ * n % 128 == 0, k % 256 == 0, m >= 0.
+ * Accuracy: per output, |y - y_exact| <= 1e-4 * sum_k |w_k * a_k| (fp32
+ * output) where a = d_a*qa, and the per-chunk integer dot products are exact.
+ * ------------------------------------------------------------------------ */
+size_t q4k_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int act);
+q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k,
+                    int act, const void* x_or_q8, const void* da_f16, const void* ssum,
+                    int64_t m, int64_t ldx,
+                    void* y, int out_dtype, int64_t ldy,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The two halves of q4k_gemm, for callers that multiply one quantized
+ * activation by several weight matrices (e.g. q, k and v of one layer).
+ * q4k_act_quantize   fp32 x [m][ldx] -> the GEMM operand form in `workspace`
+ * q4k_act_from_q8    q8 SoA (as q8_quantize_rows writes it) -> same form
+ * q4k_gemm_quantized workspace (filled by one of the two, same m and k) -> Y
+ * workspace: >= q4k_act_workspace_bytes(m, k) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t q4k_act_workspace_bytes(int64_t m, int64_t k);
+q4k_status q4k_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16_t* ssum,
+                           int64_t m, int64_t k, int64_t ldq,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k,
+                              const void* workspace, size_t workspace_bytes, int64_t m,
+                              void* y, int out_dtype, int64_t ldy, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics (these synchronise the current device).
+ * q4k_device_error_word  raw device-side error word of the current device
+ *                        (0 = none; 0x1XX = a bounded wait ran out at site XX);
+ *                        reset != 0 clears it.
+ * q4k_device_status      the same, mapped to a q4k_status.
+ * q4k_selftest_wait_timeout  launches one CTA that waits on a barrier nothing
+ *                        will complete, with the given limit (ns, 1e3..1e10),
+ *                        and returns the status the host reads back: it must
+ *                        be Q4K_ERR_TIMEOUT.  Exercises the bounded-wait path
+ *                        without faulting or hanging the GPU.
+ * q4k_gemm_debug_chunk_acc  q4k_gemm_quantized with fp32 output that also
+ *                        writes every per-chunk accumulator J[t][o][c] =
+ *                        sum_{k in chunk c} (sc*q)[o,k]*qa[t,k] (exact
+ *                        integers) to chunk_acc [m][n][k/32]; test hook,
+ *                        limited to m*n*(k/32) <= 2^26.  Asynchronous.
+ * ------------------------------------------------------------------------ */
+unsigned int q4k_device_error_word(int reset);
+q4k_status q4k_device_status(int reset);
+q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
+q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k,
+                                    const void* workspace, size_t workspace_bytes, int64_t m,
+                                    float* y, int64_t ldy, float* chunk_acc, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4K_H */

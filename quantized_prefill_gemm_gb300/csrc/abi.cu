@@ -1,0 +1,339 @@
+// Host side of the C ABI declared in include/q4k.h: argument validation,
+// buffer layouts, TMA descriptor encoding and kernel launches.  Nothing here
+// allocates device memory; only the diagnostics synchronise.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/q4k.h"
+#include "q4k_internal.h"
+#include "q4k_layout.h"
+
+namespace q4k {
+
+// Device-side error word (one per device context).  Host code must not use
+// this name as an address: the device address comes from
+// cudaGetSymbolAddress, looked up per device with that device current.
+__device__ unsigned int g_device_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4ull * 1000 * 1000 * 1000;   // 4 s per wait
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    unsigned* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+q4k_status from_cuda(cudaError_t e) { return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA; }
+
+// Per-device set-up (first call on each device, with that device current):
+// architecture check, SM count, device address of the error word.
+q4k_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return Q4K_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return Q4K_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        void* p = nullptr;
+        if (d.supported) {
+            if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return Q4K_ERR_CUDA;
+        }
+        d.err_word = static_cast<unsigned*>(p);
+        d.ready = true;
+    }
+    if (!d.supported) return Q4K_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return Q4K_OK;
+}
+
+q4k_status encoder(EncodeTiledFn* fn) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f)
+            return Q4K_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    *fn = g_encode;
+    return Q4K_OK;
+}
+
+// Row-major [rows][inner] (times `planes`) tensor, tiles of 64 inner x 128
+// rows, 128-byte swizzle, zero fill outside the tensor.
+q4k_status encode_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int64_t inner, int64_t rows,
+                      int64_t planes) {
+    EncodeTiledFn fn = nullptr;
+    q4k_status st = encoder(&fn);
+    if (st != Q4K_OK) return st;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(planes)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 2), static_cast<cuuint64_t>(inner * rows * 2)};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t rank = planes > 1 ? 3 : 2;
+    const CUresult r = fn(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+
+q4k_status check_act_f32(const float* x, int64_t m, int64_t k, int64_t ldx) {
+    if (m < 0 || k <= 0 || m >= kMaxDim || k >= kMaxDim) return Q4K_ERR_SHAPE;
+    if (k % 32) return Q4K_ERR_SHAPE;
+    if (ldx < k) return Q4K_ERR_SHAPE;
+    if (m > 0 && !x) return Q4K_ERR_INVALID_ARG;
+    if (m > 0 && (!aligned(x, 16) || ldx % 4)) return Q4K_ERR_ALIGNMENT;
+    return Q4K_OK;
+}
+
+q4k_status check_gemm_shape(int64_t n, int64_t k, int64_t m) {
+    if (n <= 0 || k <= 0 || m < 0 || n >= kMaxDim || k >= kMaxDim || m >= kMaxDim) return Q4K_ERR_SHAPE;
+    if (n % kTileN || k % 256) return Q4K_ERR_SHAPE;
+    return Q4K_OK;
+}
+
+q4k_status check_output(const void* y, int64_t m, int64_t n, int out, int64_t ldy) {
+    if (out != Q4K_OUT_F32 && out != Q4K_OUT_BF16) return Q4K_ERR_INVALID_ARG;
+    if (ldy < n) return Q4K_ERR_SHAPE;
+    if (m > 0 && !y) return Q4K_ERR_INVALID_ARG;
+    if (m > 0 && (!aligned(y, 16) || ldy % (out == Q4K_OUT_F32 ? 4 : 8))) return Q4K_ERR_ALIGNMENT;
+    return Q4K_OK;
+}
+
+q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, size_t ws_bytes, int64_t m, void* y,
+                    int out, int64_t ldy, float* dbg, cudaStream_t stream) {
+    q4k_status st = check_gemm_shape(n, k, m);
+    if (st != Q4K_OK) return st;
+    if ((st = check_output(y, m, n, out, ldy)) != Q4K_OK) return st;
+    if (!packed_w || (m > 0 && !ws)) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(packed_w, 256) || (m > 0 && !aligned(ws, 256))) return Q4K_ERR_ALIGNMENT;
+    const ActLayout A(m, k);
+    if (m > 0 && ws_bytes < static_cast<size_t>(A.total)) return Q4K_ERR_WORKSPACE;
+    if (m == 0) return Q4K_OK;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != Q4K_OK) return st;
+
+    const PackedLayout W(n, k);
+    const uint8_t* wb = static_cast<const uint8_t*>(packed_w);
+    const uint8_t* ab = static_cast<const uint8_t*>(ws);
+    const int64_t kc = k / 32;
+    CUtensorMap tm_x, tm_e, tm_d;
+    if ((st = encode_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ab + A.xq, k, m, 1)) != Q4K_OK) return st;
+    if ((st = encode_map(&tm_e, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ab + A.e, kc, m, 2)) != Q4K_OK) return st;
+    if ((st = encode_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb + W.ndm, kc, n, 2)) != Q4K_OK) return st;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.nib = wb + W.nib;
+    p.sc = wb + W.sc;
+    p.dsb = reinterpret_cast<const float*>(wb + W.dsb);
+    p.da = reinterpret_cast<const float*>(ab + A.da);
+    p.y = y;
+    p.dbg = dbg;
+    p.err = dev->err_word;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.ldy = ldy;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.kc = static_cast<int>(kc);
+    p.ksb = static_cast<int>(k / 256);
+    p.m_tiles = static_cast<int>((m + kTileM - 1) / kTileM);
+    p.n_tiles = static_cast<int>(n / kTileN);
+    p.num_tiles = p.m_tiles * p.n_tiles;
+    p.n_zst = static_cast<int>(3 * ((kc + 63) / 64));
+    p.n_main = static_cast<int>(k / 64);
+    p.out_bf16 = out == Q4K_OUT_BF16 ? 1 : 0;
+    const int grid = std::min(p.num_tiles, dev->sm_count);
+    return from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream));
+}
+
+}  // namespace
+}  // namespace q4k
+
+using namespace q4k;
+
+extern "C" {
+
+const char* q4k_status_string(int status) {
+    switch (status) {
+        case Q4K_OK: return "ok";
+        case Q4K_ERR_INVALID_ARG: return "invalid argument";
+        case Q4K_ERR_SHAPE: return "unsupported shape";
+        case Q4K_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+        case Q4K_ERR_WORKSPACE: return "workspace or packed buffer too small";
+        case Q4K_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
+        case Q4K_ERR_CUDA: return "CUDA call failed";
+        case Q4K_ERR_TIMEOUT: return "bounded device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int q4k_abi_version(void) { return Q4K_ABI_VERSION; }
+
+q4k_status q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8, uint16_t* da_f16,
+                            int16_t* ssum, cudaStream_t stream) {
+    q4k_status st = check_act_f32(x, m, k, ldx);
+    if (st != Q4K_OK) return st;
+    if (m == 0) return Q4K_OK;
+    if (!q8 || !da_f16 || !ssum) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(q8, 4) || !aligned(da_f16, 2) || !aligned(ssum, 2)) return Q4K_ERR_ALIGNMENT;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != Q4K_OK) return st;
+    return from_cuda(launch_q8_quantize_rows(x, m, k, ldx, q8, da_f16, ssum, stream));
+}
+
+size_t q4k_packed_bytes(int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0 || n % kTileN || k % 256 || n >= kMaxDim || k >= kMaxDim) return 0;
+    return static_cast<size_t>(PackedLayout(n, k).total);
+}
+
+q4k_status q4k_pack_weights(const void* blocks, int64_t n, int64_t k, void* packed, size_t packed_bytes,
+                            cudaStream_t stream) {
+    if (n <= 0 || k <= 0 || n % kTileN || k % 256 || n >= kMaxDim || k >= kMaxDim) return Q4K_ERR_SHAPE;
+    if (!blocks || !packed) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(blocks, 16) || !aligned(packed, 256)) return Q4K_ERR_ALIGNMENT;
+    if (packed_bytes < q4k_packed_bytes(n, k)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    return from_cuda(launch_pack(static_cast<const uint8_t*>(blocks), n, k, static_cast<uint8_t*>(packed), stream));
+}
+
+size_t q4k_act_workspace_bytes(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0 || k % 256 || m >= kMaxDim || k >= kMaxDim) return 0;
+    return static_cast<size_t>(ActLayout(m, k).total);
+}
+
+size_t q4k_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int act) {
+    (void)n;
+    if (act != Q4K_ACT_F32 && act != Q4K_ACT_Q8) return 0;
+    return q4k_act_workspace_bytes(m, k);
+}
+
+q4k_status q4k_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+    q4k_status st = check_act_f32(x, m, k, ldx);
+    if (st != Q4K_OK) return st;
+    if (k % 256) return Q4K_ERR_SHAPE;
+    if (m == 0) return Q4K_OK;
+    if (!workspace) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return Q4K_ERR_ALIGNMENT;
+    if (workspace_bytes < q4k_act_workspace_bytes(m, k)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != Q4K_OK) return st;
+    return from_cuda(launch_act_quantize(x, m, k, ldx, workspace, stream));
+}
+
+q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16_t* ssum, int64_t m, int64_t k,
+                           int64_t ldq, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (m < 0 || k <= 0 || k % 256 || m >= kMaxDim || k >= kMaxDim || ldq < k) return Q4K_ERR_SHAPE;
+    if (m == 0) return Q4K_OK;
+    if (!q8 || !da_f16 || !ssum || !workspace) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(q8, 4) || ldq % 4 || !aligned(da_f16, 2) || !aligned(ssum, 2) || !aligned(workspace, 256))
+        return Q4K_ERR_ALIGNMENT;
+    if (workspace_bytes < q4k_act_workspace_bytes(m, k)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    return from_cuda(launch_act_from_q8(q8, da_f16, ssum, m, k, ldq, workspace, stream));
+}
+
+q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k, const void* workspace,
+                              size_t workspace_bytes, int64_t m, void* y, int out_dtype, int64_t ldy,
+                              cudaStream_t stream) {
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, stream);
+}
+
+q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const void* x_or_q8, const void* da_f16,
+                    const void* ssum, int64_t m, int64_t ldx, void* y, int out_dtype, int64_t ldy,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    q4k_status st = check_gemm_shape(n, k, m);
+    if (st != Q4K_OK) return st;
+    if ((st = check_output(y, m, n, out_dtype, ldy)) != Q4K_OK) return st;
+    if (!packed_w) return Q4K_ERR_INVALID_ARG;
+    if (act == Q4K_ACT_F32) {
+        st = q4k_act_quantize(static_cast<const float*>(x_or_q8), m, k, ldx, workspace, workspace_bytes, stream);
+    } else if (act == Q4K_ACT_Q8) {
+        st = q4k_act_from_q8(static_cast<const int8_t*>(x_or_q8), static_cast<const uint16_t*>(da_f16),
+                             static_cast<const int16_t*>(ssum), m, k, ldx, workspace, workspace_bytes, stream);
+    } else {
+        return Q4K_ERR_INVALID_ARG;
+    }
+    if (st != Q4K_OK) return st;
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, stream);
+}
+
+unsigned int q4k_device_error_word(int reset) {
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != Q4K_OK) return 0xFFFFFFFFu;
+    if (cudaDeviceSynchronize() != cudaSuccess) return 0xFFFFFFFFu;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, dev->err_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return 0xFFFFFFFFu;
+    if (reset) {
+        const unsigned z = 0;
+        if (cudaMemcpy(dev->err_word, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return 0xFFFFFFFFu;
+    }
+    return v;
+}
+
+q4k_status q4k_device_status(int reset) {
+    const unsigned v = q4k_device_error_word(reset);
+    if (v == 0) return Q4K_OK;
+    if (v == 0xFFFFFFFFu) return Q4K_ERR_CUDA;
+    if ((v & 0xF00u) == 0x100u) return Q4K_ERR_TIMEOUT;
+    return Q4K_ERR_CUDA;
+}
+
+q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000LL) return Q4K_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    if (q4k_device_error_word(1) == 0xFFFFFFFFu) return Q4K_ERR_CUDA;
+    if (launch_selftest_wait(dev->err_word, static_cast<uint64_t>(timeout_ns), stream) != cudaSuccess)
+        return Q4K_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return Q4K_ERR_CUDA;
+    return q4k_device_status(1);
+}
+
+q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, const void* workspace,
+                                    size_t workspace_bytes, int64_t m, float* y, int64_t ldy, float* chunk_acc,
+                                    cudaStream_t stream) {
+    if (!chunk_acc) return Q4K_ERR_INVALID_ARG;
+    if (m < 0 || n <= 0 || k <= 0 || m * n * (k / 32) > (int64_t(1) << 26)) return Q4K_ERR_SHAPE;
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, Q4K_OUT_F32, ldy, chunk_acc, stream);
+}
+
+}  // extern "C"

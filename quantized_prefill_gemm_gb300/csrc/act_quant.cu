@@ -1,0 +1,202 @@
+// Activation quantization into 32-element q8 blocks.
+//
+// "34 · r31 — q-major sda scale-read repack", §1: each q8 block of the
+// activations carries an f16 scale d and an i16 ssum (the sum of its q8
+// values); the pair feeds the two-term rescale.  Rounding (the page prints
+// none): d = RN32(amax/127), inv = RN32(127/amax),
+// qa = clamp(rint_half_even(RN32(x*inv)), -127, 127), d_a = RN16(d);
+// blocks with amax < 2^-120 are zero blocks.
+//
+// One 8-lane group per block: each lane loads one float4 (4 consecutive k),
+// the group reduces amax and ssum with shuffles.  Consecutive groups take
+// consecutive blocks of the same token, so a warp reads 512 contiguous bytes.
+// HBM-bound: 4 B read per element, 1 B (public q8) or 2 B (GEMM operand)
+// written per element plus a few bytes per block.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "q4k_internal.h"
+#include "q4k_layout.h"
+
+namespace q4k {
+namespace {
+
+constexpr int kThreadsPerBlock = 256;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct LaneQ8 {
+    int q[4];
+    int ssum;       // whole block
+    __half da;      // whole block
+};
+
+__device__ __forceinline__ LaneQ8 quantize_lane(float4 v) {
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4, 8));
+    const bool live = amax >= 0x1p-120f;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __fdiv_rn(127.0f, amax);
+    LaneQ8 r;
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int q = __float2int_rn(__fmul_rn(xs[i], inv));
+        q = max(-127, min(127, q));
+        r.q[i] = live ? q : 0;
+        s += r.q[i];
+    }
+    s += __shfl_xor_sync(kFull, s, 1, 8);
+    s += __shfl_xor_sync(kFull, s, 2, 8);
+    s += __shfl_xor_sync(kFull, s, 4, 8);
+    r.ssum = s;
+    r.da = __float2half_rn(live ? d : 0.0f);
+    return r;
+}
+
+// E = d_a * ssum (exact in fp32: an 11-bit by <= 12-bit product) split into
+// two bf16 terms hi + lo with |E - hi - lo| <= 2^-16 |E|.
+__device__ __forceinline__ void split_e(__half da, int ssum, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+    const float e = __fmul_rn(__half2float(da), static_cast<float>(ssum));
+    hi = __float2bfloat16_rn(e);
+    lo = __float2bfloat16_rn(__fsub_rn(e, __bfloat162float(hi)));
+}
+
+// Public SoA output: q8 [m][k], da f16 [m][kc], ssum i16 [m][kc].
+__global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_kernel(const float* __restrict__ x, int64_t m, int64_t k,
+                                                                   int64_t ldx, int8_t* __restrict__ q8,
+                                                                   uint16_t* __restrict__ da,
+                                                                   int16_t* __restrict__ ssum) {
+    const int64_t kc = k / 32;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t grp = gid >> 3;
+    const int j = static_cast<int>(gid & 7);
+    // whole warps stay in range together: m*kc*8 is a multiple of 8, and a
+    // group's 8 lanes are consecutive, so a warp is either fully in a group
+    // range or its tail groups are all out of range
+    const bool in = grp < m * kc;
+    const int64_t t = in ? grp / kc : 0, c = in ? grp % kc : 0;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (in) v = __ldg(reinterpret_cast<const float4*>(x + t * ldx + c * 32 + 4 * j));
+    const LaneQ8 r = quantize_lane(v);
+    if (!in) return;
+    const uint32_t packed = (static_cast<uint32_t>(r.q[0]) & 0xFFu) | ((static_cast<uint32_t>(r.q[1]) & 0xFFu) << 8) |
+                            ((static_cast<uint32_t>(r.q[2]) & 0xFFu) << 16) |
+                            ((static_cast<uint32_t>(r.q[3]) & 0xFFu) << 24);
+    *reinterpret_cast<uint32_t*>(q8 + t * k + c * 32 + 4 * j) = packed;
+    if (j == 0) {
+        da[t * kc + c] = __half_as_ushort(r.da);
+        ssum[t * kc + c] = static_cast<int16_t>(r.ssum);
+    }
+}
+
+__device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64_t m, int64_t k, int64_t kc,
+                                              const int (&q)[4], __half da, int ssum, __half* __restrict__ xq,
+                                              float* __restrict__ dat, __nv_bfloat16* __restrict__ e) {
+    const __half2 h01 = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
+    const __half2 h23 = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&h01);
+    w.y = *reinterpret_cast<const uint32_t*>(&h23);
+    *reinterpret_cast<uint2*>(xq + t * k + c * 32 + 4 * j) = w;
+    if (j == 0) {
+        dat[((t >> 7) * kc + c) * 128 + (t & 127)] = __half2float(da);
+        __nv_bfloat16 hi, lo;
+        split_e(da, ssum, hi, lo);
+        e[t * kc + c] = hi;
+        e[(m + t) * kc + c] = lo;
+    }
+}
+
+// GEMM operand form (see q4k_layout.h) from fp32 activations.
+__global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float* __restrict__ x, int64_t m,
+                                                                     int64_t mp, int64_t k, int64_t ldx,
+                                                                     __half* __restrict__ xq,
+                                                                     float* __restrict__ dat,
+                                                                     __nv_bfloat16* __restrict__ e) {
+    const int64_t kc = k / 32;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t grp = gid >> 3;
+    const int j = static_cast<int>(gid & 7);
+    const bool in = grp < mp * kc;
+    const int64_t t = in ? grp / kc : 0, c = in ? grp % kc : 0;
+    const bool live_row = in && t < m;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live_row) v = __ldg(reinterpret_cast<const float4*>(x + t * ldx + c * 32 + 4 * j));
+    const LaneQ8 r = quantize_lane(v);
+    if (!in) return;
+    if (t >= m) {   // padding token of the last 128-token tile: scale 0
+        if (j == 0) dat[((t >> 7) * kc + c) * 128 + (t & 127)] = 0.0f;
+        return;
+    }
+    write_operand(t, c, j, m, k, kc, r.q, r.da, r.ssum, xq, dat, e);
+}
+
+// GEMM operand form from the public q8 SoA ([m][ldq] int8, da, ssum [m][kc]).
+__global__ void __launch_bounds__(kThreadsPerBlock) act_from_q8_kernel(const int8_t* __restrict__ q8,
+                                                                       const uint16_t* __restrict__ da,
+                                                                       const int16_t* __restrict__ ssum, int64_t m,
+                                                                       int64_t mp, int64_t k, int64_t ldq,
+                                                                       __half* __restrict__ xq,
+                                                                       float* __restrict__ dat,
+                                                                       __nv_bfloat16* __restrict__ e) {
+    const int64_t kc = k / 32;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t grp = gid >> 3;
+    const int j = static_cast<int>(gid & 7);
+    if (grp >= mp * kc) return;
+    const int64_t t = grp / kc, c = grp % kc;
+    if (t >= m) {
+        if (j == 0) dat[((t >> 7) * kc + c) * 128 + (t & 127)] = 0.0f;
+        return;
+    }
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(q8 + t * ldq + c * 32 + 4 * j));
+    int q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = static_cast<int>(static_cast<int8_t>((w >> (8 * i)) & 0xFFu));
+    const __half dh = __ushort_as_half(da[t * kc + c]);
+    write_operand(t, c, j, m, k, kc, q, dh, static_cast<int>(ssum[t * kc + c]), xq, dat, e);
+}
+
+inline unsigned grid_for(int64_t threads) {
+    return static_cast<unsigned>((threads + kThreadsPerBlock - 1) / kThreadsPerBlock);
+}
+
+}  // namespace
+
+cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8, uint16_t* da,
+                                    int16_t* ssum, cudaStream_t s) {
+    const int64_t threads = m * (k / 32) * 8;
+    if (threads == 0) return cudaSuccess;
+    q8_rows_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(x, m, k, ldx, q8, da, ssum);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s) {
+    const ActLayout L(m, k);
+    const int64_t mp = align_up(m, kTileM);
+    const int64_t threads = mp * (k / 32) * 8;
+    if (threads == 0) return cudaSuccess;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    act_quant_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(
+        x, m, mp, k, ldx, reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
+        reinterpret_cast<__nv_bfloat16*>(b + L.e));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
+                               int64_t ldq, void* ws, cudaStream_t s) {
+    const ActLayout L(m, k);
+    const int64_t mp = align_up(m, kTileM);
+    const int64_t threads = mp * (k / 32) * 8;
+    if (threads == 0) return cudaSuccess;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    act_from_q8_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(
+        q8, da, ssum, m, mp, k, ldq, reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
+        reinterpret_cast<__nv_bfloat16*>(b + L.e));
+    return cudaGetLastError();
+}
+
+}  // namespace q4k

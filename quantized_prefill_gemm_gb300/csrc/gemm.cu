@@ -1,0 +1,524 @@
+// Q4_K x q8 prefill GEMM on sm_103a tensor cores.
+//
+//   Y[t, o] = sum_sb d[o,sb] * sum_{c in sb} da[t,c] * J_c[t,o]  -  Z[t,o]
+//   J_c[t,o] = sum_{k in c} (sc*q)[o,k] * qa[t,k]          (exact integer)
+//   Z[t,o]   = sum_c (da*ssum)[t,c] * (dmin*m)[o,c]        (min term)
+//
+// This is the per-32-k integer dot product plus the two-term rank-1 rescale
+// of "34 · r31 — q-major sda scale-read repack" (§1: A-side d and ssum per
+// token and chunk; §2: B-side d*sc and -dmin*m per chunk and od row) and the
+// r15 rank-1 fold named in "22 · r17 — Wide warp remap" (§1), regrouped:
+// d*sc*I splits into sc*I (folded into the weight operand) and d (applied
+// once per super-block), and the -dmin*m*ssum*da term, a rank-1 product per
+// chunk, becomes one small GEMM of depth k/32.
+//
+// sm_103a has no integer tcgen05 MMA, so the integer dot products run on the
+// f16 kind: qa in [-127, 127] and sc*q in [0, 945] are exact fp16 integers,
+// every product is exact, and a 32-term chunk sum stays below 2^22, so the
+// fp32 TMEM accumulator holds J_c exactly.  The min-term GEMM runs in bf16 on
+// hi/lo splits of both operands (three MMAs: hi*hi + hi*lo + lo*hi, relative
+// error ~2^-16 per term, far inside the 1e-4 * sum|w*a| bound).
+//
+// One persistent CTA per SM (448 threads, 14 warps), one 128-token x 128-od
+// output tile at a time, k in stages of 64 (2 chunks of 32):
+//   warp 0        TMA producer: activation tile (fp16, 128-B swizzle), packed
+//                 quants, sc, da, d; for the min-term stages the bf16 E and
+//                 -(dmin*m) tiles
+//   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk into one of two
+//                 TMEM accumulators; 4 bf16 MMAs per min-term stage into the
+//                 tile's Y accumulator
+//   warps 2-5     converters: 4-bit quants -> fp16 sc*q written in the
+//                 128-B-swizzled K-major layout the MMA reads
+//   warps 6-13    epilogue: per chunk, P += da * J (packed fp32 FMA) from
+//                 TMEM; per super-block Y += d * P in TMEM; per tile Y -> HBM
+// TMEM (512 columns): J buffers at 0 and 128, Y buffers at 256 and 384.
+// Every wait is bounded (q4k_ptx.cuh: mbar_wait): a stuck pipeline records an
+// error word and the CTA leaves through the normal teardown.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "q4k_internal.h"
+#include "q4k_ptx.cuh"
+
+namespace q4k {
+namespace {
+
+constexpr int kStages = 5;
+constexpr int kThreads = 448;
+constexpr uint32_t kStageA = 16384;   // 128 rows x 64 fp16 / bf16
+constexpr uint32_t kStageB = 16384;
+constexpr uint32_t kStageNib = 4096;  // 2 chunks x 128 rows x 16 B
+constexpr uint32_t kStageSc = 256;    // 2 chunks x 128 rows
+constexpr uint32_t kStageDa = 1024;   // 2 chunks x 128 tokens x fp32
+constexpr uint32_t kStageD = 512;     // 128 rows x fp32 (last stage of a super-block)
+
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kStageA;
+constexpr uint32_t kOffNib = kOffB + kStages * kStageB;
+constexpr uint32_t kOffSc = kOffNib + kStages * kStageNib;
+constexpr uint32_t kOffDa = kOffSc + kStages * kStageSc;
+constexpr uint32_t kOffD = kOffDa + kStages * kStageDa;
+constexpr uint32_t kOffBar = kOffD + kStages * kStageD;
+// barrier indices
+constexpr int kBarFull = 0;                 // [kStages] producer -> all (tx bytes)
+constexpr int kBarConv = kStages;           // [kStages] converters -> MMA (4 arrivals, every stage)
+constexpr int kBarEmpty = 2 * kStages;      // [kStages] MMA commit + 8 epilogue warps -> producer
+constexpr int kBarAccFull = 3 * kStages;    // [2] MMA commit -> epilogue
+constexpr int kBarAccEmpty = kBarAccFull + 2;   // [2] 8 epilogue warps -> MMA
+constexpr int kBarZ = kBarAccEmpty + 2;     // [2] MMA commit (min term done) -> epilogue
+constexpr int kBarYEmpty = kBarZ + 2;       // [2] 8 epilogue warps -> MMA
+constexpr int kBarDrain = kBarYEmpty + 2;   // MMA's final commit
+constexpr int kNumBars = kBarDrain + 1;
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr size_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kIdescMain = idesc_kind_f16(128, 128, false);   // fp16 x fp16 -> fp32
+constexpr uint32_t kIdescMin = idesc_kind_f16(128, 128, true);     // bf16 x bf16 -> fp32
+
+// wait sites recorded in the error word
+enum : unsigned {
+    kSiteProdEmpty = 1, kSiteMmaYEmpty, kSiteMmaFull, kSiteMmaConv, kSiteMmaAccEmpty,
+    kSiteConvFull, kSiteEpiFull, kSiteEpiAccFull, kSiteEpiZ
+};
+
+struct Ctx {
+    uint32_t base;      // shared address of the 1024-aligned carve-out
+    uint8_t* sbase;     // generic pointer to the same
+    uint32_t tmem;      // TMEM base address (lane 0, column 0)
+    volatile int* abort_flag;
+    __device__ uint32_t bar(int i) const { return base + kOffBar + 8u * static_cast<uint32_t>(i); }
+    __device__ uint32_t a(int s) const { return base + kOffA + kStageA * s; }
+    __device__ uint32_t b(int s) const { return base + kOffB + kStageB * s; }
+    __device__ bool wait(const GemmParams& p, int barrier, uint32_t parity, unsigned site) const {
+        return mbar_wait(bar(barrier), parity, abort_flag, p.timeout_ns, p.err, site);
+    }
+    // all 32 lanes wait; the warp proceeds only if every lane saw the phase
+    __device__ bool warp_wait(const GemmParams& p, int barrier, uint32_t parity, unsigned site) const {
+        const bool ok = wait(p, barrier, parity, site);
+        return __all_sync(0xFFFFFFFFu, ok);
+    }
+};
+
+__device__ __forceinline__ void advance(int& s, uint32_t& ph) {
+    if (++s == kStages) {
+        s = 0;
+        ph ^= 1u;
+    }
+}
+
+// ------------------------------------------------------------- producer --
+__device__ __forceinline__ void run_producer(const Ctx& cx, const GemmParams& p, const CUtensorMap* tm_x,
+                                             const CUtensorMap* tm_e, const CUtensorMap* tm_d) {
+    const int n_st = p.n_zst + p.n_main;
+    int s = 0;
+    uint32_t ph = 0, issued = 0, parity_bits = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+        for (int st = 0; st < n_st; ++st) {
+            if (!cx.wait(p, kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = cx.bar(kBarFull + s);
+            if (st < p.n_zst) {
+                const int j = st / 3, part = st - 3 * j;   // part 0: hi*hi, 1: hi*lo, 2: lo*hi
+                mbar_arrive_expect_tx(fb, kStageA + kStageB);
+                tma_load_3d(cx.a(s), tm_e, fb, 64 * j, 128 * mt, part == 2 ? 1 : 0);
+                tma_load_3d(cx.b(s), tm_d, fb, 64 * j, 128 * nt, part == 1 ? 1 : 0);
+            } else {
+                const int kb = st - p.n_zst;
+                const bool sb_last = (kb & 3) == 3;
+                mbar_arrive_expect_tx(fb, kStageA + kStageNib + kStageSc + kStageDa + (sb_last ? kStageD : 0u));
+                tma_load_2d(cx.a(s), tm_x, fb, 64 * kb, 128 * mt);
+                const int64_t rec = static_cast<int64_t>(nt) * p.kc + 2 * kb;
+                bulk_load(cx.base + kOffNib + kStageNib * s, p.nib + rec * 128 * 16, kStageNib, fb);
+                bulk_load(cx.base + kOffSc + kStageSc * s, p.sc + rec * 128, kStageSc, fb);
+                bulk_load(cx.base + kOffDa + kStageDa * s, p.da + (static_cast<int64_t>(mt) * p.kc + 2 * kb) * 128,
+                          kStageDa, fb);
+                if (sb_last)
+                    bulk_load(cx.base + kOffD + kStageD * s,
+                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + (kb >> 2)) * 128, kStageD, fb);
+            }
+            issued |= 1u << s;
+            parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+            advance(s, ph);
+        }
+    }
+    if (!ok) {   // let every copy this thread started land before the CTA exits
+        for (int i = 0; i < kStages; ++i)
+            if ((issued >> i) & 1u) mbar_wait_quiet(cx.bar(kBarFull + i), (parity_bits >> i) & 1u, p.timeout_ns);
+    }
+}
+
+// ----------------------------------------------------------- MMA issuer --
+__device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
+    const int n_st = p.n_zst + p.n_main;
+    int s = 0, ab = 0, it = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int yb = it & 1;
+        const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!cx.wait(p, kBarYEmpty + yb, yph ^ 1u, kSiteMmaYEmpty)) break;
+        tc_fence_after();
+        const uint32_t ty = cx.tmem + 256u + 128u * yb;
+        for (int st = 0; st < n_st; ++st) {
+            if (!cx.wait(p, kBarFull + s, ph, kSiteMmaFull)) {
+                ok = false;
+                break;
+            }
+            const uint64_t ad = sw128_kmajor_desc(cx.a(s));
+            const uint64_t bd = sw128_kmajor_desc(cx.b(s));
+            if (st < p.n_zst) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
+                    tc_mma_f16(ty, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
+                tc_commit(cx.bar(kBarEmpty + s));
+                if (st == p.n_zst - 1) tc_commit(cx.bar(kBarZ + yb));
+            } else {
+                if (!cx.wait(p, kBarConv + s, ph, kSiteMmaConv)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {   // the two 32-k chunks of this stage
+                    if (!cx.wait(p, kBarAccEmpty + ab, aph ^ 1u, kSiteMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tj = cx.tmem + 128u * ab;
+                    tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
+                    tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
+                    tc_commit(cx.bar(kBarAccFull + ab));
+                    if (++ab == 2) {
+                        ab = 0;
+                        aph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(cx.bar(kBarEmpty + s));
+            }
+            advance(s, ph);
+        }
+    }
+    // every MMA this thread issued has finished before the CTA tears down
+    tc_commit(cx.bar(kBarDrain));
+    mbar_wait_quiet(cx.bar(kBarDrain), 0u, p.timeout_ns);
+}
+
+// ------------------------------------------------------------ converters --
+// Each thread owns one od row r of the tile.  For chunk h of the stage it
+// reads the row's 16 B of quants (4 words, one per 8-k group) and its sc,
+// and writes four 16-B granules of fp16 sc*q into row r of the B tile at the
+// 128-B-swizzled positions (granule g of row r lands at g ^ (r & 7)).  A
+// group of 8 consecutive lanes covers 8 consecutive rows: the 16-B reads are
+// contiguous and the granule writes fall in 8 distinct bank quads.
+__device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p, int ci, int lane) {
+    const int n_st = p.n_zst + p.n_main;
+    const int r = ci * 32 + lane;
+    const uint32_t rx = static_cast<uint32_t>(r & 7);
+    const uint32_t row_off = static_cast<uint32_t>(r >> 3) * 1024u + rx * 128u;
+    const __half2 neg1024 = __float2half2_rn(-1024.0f);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int st = 0; st < n_st; ++st) {
+            if (!cx.warp_wait(p, kBarFull + s, ph, kSiteConvFull)) {
+                ok = false;
+                break;
+            }
+            if (st < p.n_zst) {
+                // min-term stage: nothing to convert, but arrive anyway so that
+                // every stage barrier completes exactly one phase per ring pass
+                // and the MMA's phase bit stays valid for it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cx.bar(kBarConv + s));
+            } else {
+                const uint8_t* nib = cx.sbase + kOffNib + kStageNib * s;
+                const uint8_t* scs = cx.sbase + kOffSc + kStageSc * s;
+                uint8_t* brow = cx.sbase + kOffB + kStageB * s + row_off;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(nib + (h * 128 + r) * 16);
+                    const __half2 sc2 = __half2half2(__ushort2half_rn(static_cast<unsigned short>(scs[h * 128 + r])));
+                    const __half2 nsc2 = __hmul2(sc2, neg1024);   // -1024*sc, exact
+                    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            // (1024 + q) as an fp16 pair, then (1024+q)*sc - 1024*sc = sc*q
+                            // in one fused op: exact, as sc*q <= 945 is an fp16 integer
+                            const uint32_t pr = ((words[i] >> (4 * jj)) & 0x000F000Fu) | 0x64006400u;
+                            const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&pr), sc2, nsc2);
+                            o[jj] = *reinterpret_cast<const uint32_t*>(&v);
+                        }
+                        const uint32_t g = static_cast<uint32_t>(4 * h + i);
+                        *reinterpret_cast<uint4*>(brow + ((g ^ rx) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cx.bar(kBarConv + s));
+            }
+            advance(s, ph);
+        }
+    }
+}
+
+// -------------------------------------------------------------- epilogue --
+// The epilogue works on 16-column pieces (tcgen05.ld/st .x16) to keep its
+// live registers (64 partial sums + one 16-value piece) within the budget
+// of a 448-thread CTA.
+__device__ __forceinline__ void store_row16(const GemmParams& p, int64_t t, int col, const uint32_t (&v)[16]) {
+    if (p.out_bf16) {
+        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + t * p.ldy + col;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 pr =
+                    __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * i]), __uint_as_float(v[8 * q + 2 * i + 1]));
+                w[i] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            *reinterpret_cast<uint4*>(y + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        float* y = static_cast<float*>(p.y) + t * p.ldy + col;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(y + 4 * q) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+}
+
+__device__ __forceinline__ void dump_chunk(const GemmParams& p, int64_t t, int col, int64_t c, const uint32_t (&J)[16]) {
+    if (t >= p.m) return;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) p.dbg[(t * p.n + col + j) * p.kc + c] = __uint_as_float(J[j]);
+}
+
+// Warp e (0..7) reads TMEM lanes 32*(warp%4)..+31 (the lane quadrant its
+// warp index allows) and columns 64*(e/4)..+63 of each buffer: each thread
+// owns one token row and 64 output columns.
+template <bool kDump>
+__device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p, int warp, int e, int lane) {
+    const int n_st = p.n_zst + p.n_main;
+    const int qd = warp & 3, ch = e >> 2;
+    const int row = qd * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    int s = 0, ab = 0, it = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+        const int yb = it & 1;
+        const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
+        const uint32_t ty = cx.tmem + lane_off + 256u + 128u * yb + 64u * ch;
+        const int64_t t = static_cast<int64_t>(mt) * 128 + row;
+        const int col0 = nt * 128 + 64 * ch;
+        float P[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) P[j] = 0.0f;
+        bool zready = false;
+        for (int st = 0; ok && st < n_st; ++st) {
+            if (!cx.warp_wait(p, kBarFull + s, ph, kSiteEpiFull)) {
+                ok = false;
+                break;
+            }
+            if (st >= p.n_zst) {
+                const int kb = st - p.n_zst;
+                const float* das = reinterpret_cast<const float*>(cx.sbase + kOffDa + kStageDa * s);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float da = das[h * 128 + row];
+                    if (ok && !cx.warp_wait(p, kBarAccFull + ab, aph, kSiteEpiAccFull)) ok = false;
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t tj = cx.tmem + lane_off + 128u * ab + 64u * ch;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t J[16];
+                            tmem_ld16(tj + 16u * q, J);
+                            tmem_wait_ld();
+                            if (q == 3) {   // whole buffer read: hand it back to the MMA
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(cx.bar(kBarAccEmpty + ab));
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; j += 2)
+                                ffma2(P[16 * q + j], P[16 * q + j + 1], da, da, __uint_as_float(J[j]),
+                                      __uint_as_float(J[j + 1]));
+                            if (kDump) dump_chunk(p, t, col0 + 16 * q, 2 * kb + h, J);
+                        }
+                    }
+                    if (++ab == 2) {
+                        ab = 0;
+                        aph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if ((kb & 3) == 3) {   // super-block done: Y += d * P
+                    if (!zready) {
+                        if (!cx.warp_wait(p, kBarZ + yb, yph, kSiteEpiZ)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        zready = true;
+                    }
+                    const float* dv = reinterpret_cast<const float*>(cx.sbase + kOffD + kStageD * s) + 64 * ch;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t Yv[16];
+                        tmem_ld16(ty + 16u * q, Yv);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 d4 = *reinterpret_cast<const float4*>(dv + 16 * q + j);
+                            Yv[j] = __float_as_uint(fmaf(d4.x, P[16 * q + j], __uint_as_float(Yv[j])));
+                            Yv[j + 1] = __float_as_uint(fmaf(d4.y, P[16 * q + j + 1], __uint_as_float(Yv[j + 1])));
+                            Yv[j + 2] = __float_as_uint(fmaf(d4.z, P[16 * q + j + 2], __uint_as_float(Yv[j + 2])));
+                            Yv[j + 3] = __float_as_uint(fmaf(d4.w, P[16 * q + j + 3], __uint_as_float(Yv[j + 3])));
+                        }
+                        tmem_st16(ty + 16u * q, Yv);
+                    }
+                    tmem_wait_st();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) P[j] = 0.0f;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bar(kBarEmpty + s));
+            advance(s, ph);
+        }
+        if (!ok) break;
+        // tile done: Y (TMEM) -> HBM
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t Yv[16];
+            tmem_ld16(ty + 16u * q, Yv);
+            tmem_wait_ld();
+            if (t < p.m) store_row16(p, t, col0 + 16 * q, Yv);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
+    }
+}
+
+// kDump: also write every per-chunk accumulator to p.dbg (test hook build).
+template <bool kDump>
+__global__ void __launch_bounds__(kThreads, 1)
+    q4k_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_e,
+                    const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    Ctx cx;
+    cx.base = base;
+    cx.sbase = smem_raw + (base - raw);
+    cx.abort_flag = reinterpret_cast<volatile int*>(cx.sbase + kOffMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(cx.bar(kBarFull + s), 1);
+            mbar_init(cx.bar(kBarConv + s), 4);
+            mbar_init(cx.bar(kBarEmpty + s), 9);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(cx.bar(kBarAccFull + b), 1);
+            mbar_init(cx.bar(kBarAccEmpty + b), 8);
+            mbar_init(cx.bar(kBarZ + b), 1);
+            mbar_init(cx.bar(kBarYEmpty + b), 8);
+        }
+        mbar_init(cx.bar(kBarDrain), 1);
+        *cx.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(base + kOffMisc, 512);
+    if (warp == 1 && lane == 0) {
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_e);
+        prefetch_tmap(&tm_d);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.sbase + kOffMisc);
+
+    if (warp == 0) {
+        if (lane == 0) run_producer(cx, p, &tm_x, &tm_e, &tm_d);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) run_mma(cx, p);
+        __syncwarp();
+    } else if (warp < 6) {
+        run_converter(cx, p, warp - 2, lane);
+    } else {
+        run_epilogue<kDump>(cx, p, warp, warp - 6, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(cx.tmem, 512);
+    }
+}
+
+// Bounded-wait self-test: one CTA waits on a barrier nothing completes.
+__global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait(smem_u32(&bar), 0u, &abort_flag, timeout_ns, err, 0x20u);
+    __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
+                        const GemmParams& p, int grid, cudaStream_t s) {
+    static bool attr_set[64][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int dump = p.dbg != nullptr ? 1 : 0;
+    if (!attr_set[dev][dump]) {
+        e = dump ? cudaFuncSetAttribute(q4k_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemBytes))
+                 : cudaFuncSetAttribute(q4k_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set[dev][dump] = true;
+    }
+    if (dump)
+        q4k_gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
+    else
+        q4k_gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_ns, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace q4k

@@ -1,0 +1,36 @@
+// Launch wrappers shared by the library's translation units (not exported).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4k {
+
+struct GemmParams {
+    const uint8_t* nib;     // packed quants  [nt][kc][128][16 B]
+    const uint8_t* sc;      // packed scales  [nt][kc][128]
+    const float* dsb;       // super-block d  [nt][ksb][128]
+    const float* da;        // token scales   [mp/128][kc][128]
+    void* y;                // output [m][ldy]
+    float* dbg;             // optional per-chunk accumulators [m][n][kc] (test hook)
+    unsigned* err;          // device error word
+    uint64_t timeout_ns;    // bound of every internal wait
+    int64_t ldy;
+    int m, n, k;
+    int kc, ksb;
+    int m_tiles, n_tiles, num_tiles;
+    int n_zst, n_main;      // min-term stages and main stages per tile
+    int out_bf16;
+};
+
+cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8,
+                                    uint16_t* da, int16_t* ssum, cudaStream_t s);
+cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s);
+cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
+                               int64_t ldq, void* ws, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
+cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
+                        const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace q4k
