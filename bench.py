@@ -196,10 +196,12 @@ def main():
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     start.record(stream)
     for s in range(args.steps):
         step(ev[s])
     stop.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     clk = clocks.stop()
     total_ms = start.elapsed_time(stop)
@@ -252,7 +254,11 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2)
     """Same metric through the public fused call q4k_gemm, with every
     projection's activations copied from pinned host memory and its result
     copied back inside the timed region."""
-    host_x = [x.cpu().pin_memory() for x in xs]
+    host_x = []
+    for x in xs:
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hx.copy_(x)
+        host_x.append(hx)
     ydt = torch.bfloat16 if out == "bf16" else torch.float32
     host_y = [torch.empty((tokens, n), dtype=ydt, pin_memory=True) for n, _ in mats]
     dx = {k: torch.empty((tokens, k), dtype=torch.float32, device=dev) for _, k in mats}
