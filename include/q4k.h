@@ -144,6 +144,37 @@ q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k,
                               void* y, int out_dtype, int64_t ldy, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * q4k_gemm_static_workspace -- q4k_gemm without a workspace argument.
+ * Library addition with no counterpart in the pages: it exists for callers
+ * that cannot hand the library scratch memory, e.g. a plain C host that holds
+ * only its input and output pointers, or an engine that carves its device
+ * memory once at start-up and must not call cudaMalloc afterwards (cudaMalloc
+ * can synchronise the device).  It allocates nothing: the activation
+ * workspace is a fixed array of Q4K_STATIC_WORKSPACE_BYTES in the library's
+ * own device memory (one per device context, alive while the library is
+ * loaded).
+ *   Arguments, layouts and results: as q4k_gemm (same kernels, so the output
+ *   is identical to q4k_gemm's on the same inputs).
+ *   Limit: q4k_gemm_workspace_bytes(m, n, k, act) must not exceed
+ *   Q4K_STATIC_WORKSPACE_BYTES (64 MiB: e.g. m = 2048 tokens at k = 11008);
+ *   larger problems return Q4K_ERR_WORKSPACE before anything is launched.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress, with that device current); make that
+ *   first call before any stream capture on the device.
+ *   Sharing: all calls on one device use the same array and leave the last
+ *   call's contents in it.  Calls that overlap in time on one device (other
+ *   streams, other host threads) race on it; the caller must order them.
+ *   Nothing in it needs clearing: each call rewrites what it reads.
+ * q4k_static_workspace_bytes returns Q4K_STATIC_WORKSPACE_BYTES.
+ * ------------------------------------------------------------------------ */
+#define Q4K_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+size_t q4k_static_workspace_bytes(void);
+q4k_status q4k_gemm_static_workspace(const void* packed_w, int64_t n, int64_t k,
+                                     int act, const void* x_or_q8, const void* da_f16,
+                                     const void* ssum, int64_t m, int64_t ldx,
+                                     void* y, int out_dtype, int64_t ldy, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics (these synchronise the current device).
  * q4k_device_error_word  raw device-side error word of the current device
  *                        (0 = none; 0x1XX = a bounded wait ran out at site XX);

@@ -45,6 +45,9 @@ SIGNATURES = {
     "q4k_selftest_wait_timeout": (_c_int, [_c_i64, _c_ptr]),
     "q4k_gemm_debug_chunk_acc": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_i64,
                                           _c_ptr, _c_ptr]),
+    "q4k_static_workspace_bytes": (_c_size, []),
+    "q4k_gemm_static_workspace": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
+                                           _c_ptr, _c_int, _c_i64, _c_ptr]),
 }
 
 
@@ -197,6 +200,29 @@ def q4k_gemm(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, out_dtype="f
         _dev(da, "da", torch.float16) if act == ACT_Q8 else None,
         _dev(ssum, "ssum", torch.int16) if act == ACT_Q8 else None,
         m, ldx, _dev(y, "y"), code, ldy, _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return y
+
+
+def q4k_static_workspace_bytes() -> int:
+    return int(LIB.q4k_static_workspace_bytes())
+
+
+def q4k_gemm_static_workspace(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, y: torch.Tensor,
+                              da=None, ssum=None, stream=None) -> torch.Tensor:
+    """q4k_gemm into the caller's y (fp32 or bf16 [m][n..]) with the library's own fixed
+    workspace: nothing is allocated, here or in the library."""
+    m, kx, ldx = _row_major(x, "x")
+    if kx != k:
+        raise ValueError("x has the wrong number of columns")
+    act = ACT_Q8 if x.dtype == torch.int8 else ACT_F32
+    if act == ACT_Q8 and (da is None or ssum is None):
+        raise ValueError("q8 input needs da and ssum")
+    code, y, ldy = _out(m, n, y.dtype, y, x.device)
+    _check("q4k_gemm_static_workspace", LIB.q4k_gemm_static_workspace(
+        _dev(packed, "packed"), n, k, act, _dev(x, "x"),
+        _dev(da, "da", torch.float16) if act == ACT_Q8 else None,
+        _dev(ssum, "ssum", torch.int16) if act == ACT_Q8 else None,
+        m, ldx, _dev(y, "y"), code, ldy, _stream(stream)))
     return y
 
 
