@@ -24,6 +24,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 4ull * 1000 * 1000 * 1000;   // 4 s per wait
+// waits are bounded in SM cycles; 2 cycles per ns keeps the bound >= the
+// nominal time at any clock up to 2 GHz (longer at lower clocks)
+constexpr uint64_t kCyclesPerNs = 2;
 
 struct DeviceInfo {
     bool ready = false;
@@ -162,7 +165,7 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
     p.y = y;
     p.dbg = dbg;
     p.err = dev->err_word;
-    p.timeout_ns = kDefaultTimeoutNs;
+    p.timeout_cycles = kDefaultTimeoutNs * kCyclesPerNs;
     p.ldy = ldy;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
@@ -322,7 +325,7 @@ q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
     q4k_status st = device_info(&dev);
     if (st != Q4K_OK) return st;
     if (q4k_device_error_word(1) == 0xFFFFFFFFu) return Q4K_ERR_CUDA;
-    if (launch_selftest_wait(dev->err_word, static_cast<uint64_t>(timeout_ns), stream) != cudaSuccess)
+    if (launch_selftest_wait(dev->err_word, static_cast<uint64_t>(timeout_ns) * kCyclesPerNs, stream) != cudaSuccess)
         return Q4K_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return Q4K_ERR_CUDA;
     return q4k_device_status(1);

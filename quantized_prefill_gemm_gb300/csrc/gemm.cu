@@ -92,7 +92,7 @@ struct Ctx {
     __device__ uint32_t a(int s) const { return base + kOffA + kStageA * s; }
     __device__ uint32_t b(int s) const { return base + kOffB + kStageB * s; }
     __device__ bool wait(const GemmParams& p, int barrier, uint32_t parity, unsigned site) const {
-        return mbar_wait(bar(barrier), parity, abort_flag, p.timeout_ns, p.err, site);
+        return mbar_wait(bar(barrier), parity, abort_flag, p.timeout_cycles, p.err, site);
     }
     // all 32 lanes wait; the warp proceeds only if every lane saw the phase
     __device__ bool warp_wait(const GemmParams& p, int barrier, uint32_t parity, unsigned site) const {
@@ -149,7 +149,7 @@ __device__ __forceinline__ void run_producer(const Ctx& cx, const GemmParams& p,
     }
     if (!ok) {   // let every copy this thread started land before the CTA exits
         for (int i = 0; i < kStages; ++i)
-            if ((issued >> i) & 1u) mbar_wait_quiet(cx.bar(kBarFull + i), (parity_bits >> i) & 1u, p.timeout_ns);
+            if ((issued >> i) & 1u) mbar_wait_quiet(cx.bar(kBarFull + i), (parity_bits >> i) & 1u, p.timeout_cycles);
     }
 }
 
@@ -209,7 +209,7 @@ __device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
     }
     // every MMA this thread issued has finished before the CTA tears down
     tc_commit(cx.bar(kBarDrain));
-    mbar_wait_quiet(cx.bar(kBarDrain), 0u, p.timeout_ns);
+    mbar_wait_quiet(cx.bar(kBarDrain), 0u, p.timeout_cycles);
 }
 
 // ------------------------------------------------------------ converters --
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Bounded-wait self-test: one CTA waits on a barrier nothing completes.
-__global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_ns) {
+__global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_cycles) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -487,7 +487,7 @@ __global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_ns) {
         fence_mbar_init();
     }
     __syncthreads();
-    mbar_wait(smem_u32(&bar), 0u, &abort_flag, timeout_ns, err, 0x20u);
+    mbar_wait(smem_u32(&bar), 0u, &abort_flag, timeout_cycles, err, 0x20u);
     __syncthreads();
 }
 
@@ -516,8 +516,8 @@ cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_ns, cudaStream_t s) {
-    selftest_wait_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 32, 0, s>>>(err, timeout_cycles);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,7 @@ struct GemmParams {
     void* y;                // output [m][ldy]
     float* dbg;             // optional per-chunk accumulators [m][n][kc] (test hook)
     unsigned* err;          // device error word
-    uint64_t timeout_ns;    // bound of every internal wait
+    uint64_t timeout_cycles;   // bound of every internal wait, in SM clock cycles
     int64_t ldy;
     int m, n, k;
     int kc, ksb;
@@ -31,6 +31,6 @@ cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16
 cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                         const GemmParams& p, int grid, cudaStream_t s);
-cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_ns, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s);
 
 }  // namespace q4k

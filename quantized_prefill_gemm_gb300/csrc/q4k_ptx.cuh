@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -44,19 +38,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As above, but a thread whose phase is not complete sleeps (without issuing)
+// until the phase completes or kSuspendHintNs pass, instead of returning at
+// once: waiting warps then leave the issue slots to the warps doing work.
+constexpr uint32_t kSuspendHintNs = 1000000;   // 1 ms
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
 
-// Wait for phase `parity` of `bar` to complete, for at most timeout_ns.
-// Gives up early when another thread of the CTA raised *abort.  On a timeout
-// it records kErrTimeoutBase|site in the device error word, raises *abort and
-// returns false; the caller then leaves its loops and joins the teardown.
+// Non-blocking test of phase `parity` (no suspension).  On a completed phase
+// it answers in ~15 cycles even while the tensor core saturates the shared
+// memory read port, where a plain ld.shared takes ~100.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, for at most `timeout` SM
+// clock cycles.  Gives up early when another thread of the CTA raised *abort.
+// On a timeout it records kErrTimeoutBase|site in the device error word,
+// raises *abort and returns false; the caller then leaves its loops and joins
+// the teardown.  The limit uses the SM's own cycle counter (read in a few
+// cycles).  backoff_ns > 0 sleeps that long between polls: a role that is not
+// on the critical path then leaves the issue slots of its SM sub-partition to
+// the warps that are (a spinning warp is always ready to issue).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                       uint64_t timeout_ns, unsigned* err, unsigned site) {
+                                          uint64_t timeout, unsigned* err, unsigned site,
+                                          uint32_t backoff_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (true) {
+        if (backoff_ns) __nanosleep(backoff_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) {
+        if (static_cast<uint64_t>(clock64() - t0) > timeout) {
             atomicCAS(err, 0u, kErrTimeoutBase | site);
             *abort = 1;
             return false;
@@ -65,10 +95,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Same, ignoring the abort flag (teardown: wait for own copies in flight).
-__device__ __noinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
+__device__ __noinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t timeout) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait_sleep(bar, parity)) {
+        if (static_cast<uint64_t>(clock64() - t0) > timeout) return false;
     }
     return true;
 }
@@ -209,6 +239,34 @@ __device__ __forceinline__ void ffma2(float& c0, float& c1, float a0, float a1, 
         "mov.b64 {%0, %1}, rc;\n\t}"
         : "+f"(c0), "+f"(c1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Warpgroup register re-split (all four warps of a warpgroup execute the same
+// one).  .inc waits until other warpgroups' .dec have returned registers, so
+// the shares must add up to at most the CTA's launch allocation.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// Packed-pair forms: a 64-bit register holds two fp32 values (low = first).
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, uint32_t& lo, uint32_t& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+// d = a * b + c on both halves, round to nearest.
+__device__ __forceinline__ uint64_t ffma2_pk(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
 }  // namespace q4k
