@@ -117,7 +117,14 @@ q4k_status q4k_pack_weights(const void* q4k_blocks, int64_t n, int64_t k,
  * n % 128 == 0, k % 256 == 0, m >= 0.
  * Accuracy: per output, |y - y_exact| <= 1e-4 * sum_k |w_k * a_k| (fp32
  * output) where a = d_a*qa, and the per-chunk integer dot products are exact.
+ * Small M: for 1 <= m <= Q4K_SMALL_M tokens (decode-sized batches) the call
+ * runs a CUDA-core kernel whose cost is reading the packed weights (integer
+ * dot products with dp4a, same rescale and accuracy contract); the f32 path
+ * then uses the first bytes of `workspace` for the q8 SoA, and the q8 path
+ * reads the caller's arrays directly when q8, da_f16 and ssum are 16-byte
+ * aligned and ldx % 16 == 0 (otherwise it takes the general path).
  * ------------------------------------------------------------------------ */
+#define Q4K_SMALL_M 16
 size_t q4k_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int act);
 q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k,
                     int act, const void* x_or_q8, const void* da_f16, const void* ssum,

@@ -182,6 +182,49 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
     return from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream));
 }
 
+// Small-M path: the q8 SoA (q8 rows, d_a and ssum 16-byte aligned, ldq % 16 ==
+// 0) times the packed weights on the CUDA cores.
+q4k_status run_gemv(const void* packed_w, int64_t n, int64_t k, const int8_t* q8, const uint16_t* da,
+                    const int16_t* ssum, int64_t m, int64_t ldq, void* y, int out, int64_t ldy, cudaStream_t stream) {
+    DeviceInfo* dev = nullptr;
+    q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    const PackedLayout W(n, k);
+    const uint8_t* wb = static_cast<const uint8_t*>(packed_w);
+    GemvParams g;
+    std::memset(&g, 0, sizeof(g));
+    g.nib = wb + W.nib;
+    g.sc = wb + W.sc;
+    g.mq = wb + W.mq;
+    g.dsb = reinterpret_cast<const float*>(wb + W.dsb);
+    g.dmn = reinterpret_cast<const float*>(wb + W.dmn);
+    g.q8 = q8;
+    g.da = da;
+    g.ssum = ssum;
+    g.y = y;
+    g.ldq = ldq;
+    g.ldy = ldy;
+    g.m = static_cast<int>(m);
+    g.n = static_cast<int>(n);
+    g.k = static_cast<int>(k);
+    g.kc = static_cast<int>(k / 32);
+    g.ksb = static_cast<int>(k / 256);
+    g.out_bf16 = out == Q4K_OUT_BF16 ? 1 : 0;
+    return from_cuda(launch_gemv(g, stream));
+}
+
+// Where the small-M path keeps the q8 SoA inside a q4k_gemm workspace.
+struct SmallMLayout {
+    int64_t q8, da, ssum, total;
+    SmallMLayout(int64_t m, int64_t k) {
+        const int64_t kc = k / 32;
+        q8 = 0;
+        da = align_up(m * k, 256);
+        ssum = align_up(da + m * kc * 2, 256);
+        total = align_up(ssum + m * kc * 2, 256);
+    }
+};
+
 }  // namespace
 }  // namespace q4k
 
@@ -286,13 +329,36 @@ q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
     if (st != Q4K_OK) return st;
     if ((st = check_output(y, m, n, out_dtype, ldy)) != Q4K_OK) return st;
     if (!packed_w) return Q4K_ERR_INVALID_ARG;
+    if (act != Q4K_ACT_F32 && act != Q4K_ACT_Q8) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(packed_w, 256)) return Q4K_ERR_ALIGNMENT;
+    if (m >= 1 && m <= Q4K_SMALL_M) {   // decode-sized: CUDA-core path, bound by the weight stream
+        if (act == Q4K_ACT_F32) {
+            if ((st = check_act_f32(static_cast<const float*>(x_or_q8), m, k, ldx)) != Q4K_OK) return st;
+            const SmallMLayout L(m, k);
+            if (!workspace) return Q4K_ERR_INVALID_ARG;
+            if (!aligned(workspace, 256)) return Q4K_ERR_ALIGNMENT;
+            if (workspace_bytes < static_cast<size_t>(L.total)) return Q4K_ERR_WORKSPACE;
+            uint8_t* wsb = static_cast<uint8_t*>(workspace);
+            int8_t* q8 = reinterpret_cast<int8_t*>(wsb + L.q8);
+            uint16_t* da = reinterpret_cast<uint16_t*>(wsb + L.da);
+            int16_t* ss = reinterpret_cast<int16_t*>(wsb + L.ssum);
+            st = q8_quantize_rows(static_cast<const float*>(x_or_q8), m, k, ldx, q8, da, ss, stream);
+            if (st != Q4K_OK) return st;
+            return run_gemv(packed_w, n, k, q8, da, ss, m, k, y, out_dtype, ldy, stream);
+        }
+        const int8_t* q8 = static_cast<const int8_t*>(x_or_q8);
+        if (!q8 || !da_f16 || !ssum) return Q4K_ERR_INVALID_ARG;
+        if (ldx < k) return Q4K_ERR_SHAPE;
+        if (aligned(q8, 16) && ldx % 16 == 0 && aligned(da_f16, 16) && aligned(ssum, 16))
+            return run_gemv(packed_w, n, k, q8, static_cast<const uint16_t*>(da_f16),
+                            static_cast<const int16_t*>(ssum), m, ldx, y, out_dtype, ldy, stream);
+        // other alignments go through the general path below
+    }
     if (act == Q4K_ACT_F32) {
         st = q4k_act_quantize(static_cast<const float*>(x_or_q8), m, k, ldx, workspace, workspace_bytes, stream);
-    } else if (act == Q4K_ACT_Q8) {
+    } else {
         st = q4k_act_from_q8(static_cast<const int8_t*>(x_or_q8), static_cast<const uint16_t*>(da_f16),
                              static_cast<const int16_t*>(ssum), m, k, ldx, workspace, workspace_bytes, stream);
-    } else {
-        return Q4K_ERR_INVALID_ARG;
     }
     if (st != Q4K_OK) return st;
     return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, stream);

@@ -1,0 +1,210 @@
+// Small-M (decode-sized) Q4_K x q8 product: m <= 16 tokens.
+//
+// The same arithmetic as the GEMM ("34 · r31 — q-major sda scale-read
+// repack", §1-§2: per 32-k chunk an exact integer dot product, then the
+// two-term rescale d_a*(d*sc)*sum(q*qa) + d_a*ssum*(-dmin*m)), but with so few
+// tokens the product is bound by reading the packed weights from HBM, not by
+// the tensor cores.  So it runs on the CUDA cores: the integer dot products
+// with dp4a on 4-bit quants unpacked to bytes, the rescale in fp32.
+//
+// One CTA per 16 od rows (grid = n / 16), 256 threads.  Lane l of warp w owns
+// row l % 16 and super-blocks s with s % 16 == 2 * w + l / 16, so a half-warp
+// reads 16 consecutive rows' 16-B quant records of one chunk (256 contiguous
+// bytes).  For each super-block the half-warp first copies the activations
+// it needs (q8 bytes, d_a and ssum of the super-block's 8 chunks, for every
+// token) into its own shared-memory stage with 16-B loads, while the quants
+// of the next super-block are already on their way into registers; all 16
+// lanes then read the stage (broadcast).  The 16 partial sums of a row are
+// added in shared memory in a fixed order (deterministic), then stored.
+//
+// Per thread and chunk: J[t] = sum_{k in chunk} q[k] * qa[t][k] (exact,
+// dp4a), P[t] += d_a[t] * (sc * J[t]) (sc*J < 2^22 is exact in fp32),
+// Z[t] += (d_a[t] * ssum[t]) * (-dmin * m) (both factors exact in fp32); per
+// super-block Y[t] += d * P[t].
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "q4k_internal.h"
+
+namespace q4k {
+namespace {
+
+constexpr int kRows = 16;      // od rows per CTA
+constexpr int kParts = 16;     // super-block shares per row (2 per warp)
+constexpr int kThreads = 256;
+
+// 4-bit quants of one 8-k group (one packed word) -> two words of 4 bytes in
+// k order.  In the packed word the nibble at bits 4j is k = 2j and the nibble
+// at bits 16 + 4j is k = 2j + 1.
+__device__ __forceinline__ void unpack_group(uint32_t w, uint32_t& k0123, uint32_t& k4567) {
+    const uint32_t a = w & 0x000F000Fu;           // bytes 0, 2: k0, k1
+    const uint32_t b = (w >> 4) & 0x000F000Fu;    // bytes 0, 2: k2, k3
+    const uint32_t c = (w >> 8) & 0x000F000Fu;    // k4, k5
+    const uint32_t e = (w >> 12) & 0x000F000Fu;   // k6, k7
+    k0123 = __byte_perm(a, b, 0x6420);
+    k4567 = __byte_perm(c, e, 0x6420);
+}
+
+// Activations of one super-block for M tokens.
+template <int M>
+struct Stage {
+    int4 qa[M][16];   // q8 bytes of the 256 k
+    uint4 da[M];      // d_a of the 8 chunks (f16 bits)
+    uint4 ss[M];      // ssum of the 8 chunks
+};
+
+template <int M>
+constexpr size_t gemv_smem_bytes() {
+    return kParts * sizeof(Stage<M>) > kParts * M * kRows * sizeof(float) ? kParts * sizeof(Stage<M>)
+                                                                           : kParts * M * kRows * sizeof(float);
+}
+
+// 8 chunks' quants, sc and m of one (row, super-block)
+struct SbWeights {
+    uint4 q[8];
+    uint32_t scm[8];   // sc | m << 8
+};
+
+__device__ __forceinline__ void load_weights(const GemvParams& p, int64_t nt, int64_t r, int sb, SbWeights& w) {
+    const int64_t rec0 = (nt * p.kc + 8 * sb) * 128 + r;   // chunk 8*sb of this row
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        w.q[j] = __ldg(reinterpret_cast<const uint4*>(p.nib) + rec0 + 128 * j);
+        w.scm[j] = static_cast<uint32_t>(__ldg(p.sc + rec0 + 128 * j)) |
+                   (static_cast<uint32_t>(__ldg(p.mq + rec0 + 128 * j)) << 8);
+    }
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const GemvParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Stage<M>* stages = reinterpret_cast<Stage<M>*>(smem_raw);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hl = lane & 15;                    // row within the CTA / lane within the half-warp
+    const int part = 2 * warp + (lane >> 4);     // super-block share
+    const int64_t o = static_cast<int64_t>(blockIdx.x) * kRows + hl;
+    const int64_t nt = o >> 7, r = o & 127;
+    const int kc = p.kc, ksb = p.ksb, m = p.m;
+    Stage<M>& st = stages[part];
+
+    float acc[M];
+#pragma unroll
+    for (int t = 0; t < M; ++t) acc[t] = 0.0f;
+
+    // Every lane runs the same number of rounds (the two half-warps of a warp
+    // may have different numbers of super-blocks): the warp-wide __syncwarp
+    // below is then reached by all 32 lanes; a lane without a super-block in
+    // a round only takes part in the synchronisation.
+    const int rounds = (ksb + kParts - 1) / kParts;
+    SbWeights cur, nxt;
+    if (part < ksb) load_weights(p, nt, r, part, cur);
+    for (int round = 0; round < rounds; ++round) {
+        const int sb = part + round * kParts;
+        const bool active = sb < ksb;
+        if (!active) {   // nothing to do this round but the two warp barriers
+            __syncwarp();
+            __syncwarp();
+            continue;
+        }
+        // stage this super-block's activations (the half-warp shares them)
+#pragma unroll
+        for (int t = 0; t < M; ++t)
+            if (t < m) st.qa[t][hl] = __ldg(reinterpret_cast<const int4*>(p.q8 + t * p.ldq + 256 * sb) + hl);
+        if (hl < m && hl < M) {
+            st.da[hl] = __ldg(reinterpret_cast<const uint4*>(p.da + hl * kc + 8 * sb));
+            st.ss[hl] = __ldg(reinterpret_cast<const uint4*>(p.ssum + hl * kc + 8 * sb));
+        }
+        if (sb + kParts < ksb) load_weights(p, nt, r, sb + kParts, nxt);   // in flight during this one
+        const int64_t srec = (nt * ksb + sb) * 128 + r;
+        const float d = __ldg(p.dsb + srec);
+        const float dmin = __ldg(p.dmn + srec);
+        __syncwarp();
+        float P[M], Z[M];
+#pragma unroll
+        for (int t = 0; t < M; ++t) {
+            P[t] = 0.0f;
+            Z[t] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t q[8];
+            unpack_group(cur.q[j].x, q[0], q[1]);
+            unpack_group(cur.q[j].y, q[2], q[3]);
+            unpack_group(cur.q[j].z, q[4], q[5]);
+            unpack_group(cur.q[j].w, q[6], q[7]);
+            const int sc = static_cast<int>(cur.scm[j] & 0xFFu);
+            const float nm = -(dmin * static_cast<float>(cur.scm[j] >> 8));   // exact: f16 value x 6-bit m
+#pragma unroll
+            for (int t = 0; t < M; ++t) {
+                if (t < m) {
+                    const int4 a0 = st.qa[t][2 * j], a1 = st.qa[t][2 * j + 1];
+                    int J = __dp4a(static_cast<int>(q[0]), a0.x, 0);
+                    J = __dp4a(static_cast<int>(q[1]), a0.y, J);
+                    J = __dp4a(static_cast<int>(q[2]), a0.z, J);
+                    J = __dp4a(static_cast<int>(q[3]), a0.w, J);
+                    J = __dp4a(static_cast<int>(q[4]), a1.x, J);
+                    J = __dp4a(static_cast<int>(q[5]), a1.y, J);
+                    J = __dp4a(static_cast<int>(q[6]), a1.z, J);
+                    J = __dp4a(static_cast<int>(q[7]), a1.w, J);
+                    const float da =
+                        __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(&st.da[t])[j]));
+                    const float ss = static_cast<float>(reinterpret_cast<const int16_t*>(&st.ss[t])[j]);
+                    P[t] = fmaf(da, static_cast<float>(sc * J), P[t]);
+                    Z[t] = fmaf(da * ss, nm, Z[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < M; ++t) acc[t] = fmaf(d, P[t], acc[t]) + Z[t];
+        __syncwarp();   // the stage is read by every lane before the next super-block overwrites it
+        cur = nxt;
+    }
+
+    // add the 16 shares of each row in a fixed order (the stages are free now)
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(smem_raw);   // [kParts][M][kRows]
+#pragma unroll
+    for (int t = 0; t < M; ++t) red[(part * M + t) * kRows + hl] = acc[t];
+    __syncthreads();
+    for (int i = threadIdx.x; i < M * kRows; i += kThreads) {
+        const int t = i / kRows, rr = i % kRows;
+        if (t >= m) continue;
+        float v = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kParts; ++s) v += red[(s * M + t) * kRows + rr];
+        const int64_t oo = static_cast<int64_t>(blockIdx.x) * kRows + rr;
+        if (p.out_bf16)
+            static_cast<__nv_bfloat16*>(p.y)[t * p.ldy + oo] = __float2bfloat16_rn(v);
+        else
+            static_cast<float*>(p.y)[t * p.ldy + oo] = v;
+    }
+}
+
+template <int M>
+cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    constexpr size_t smem = gemv_smem_bytes<M>();
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(q4k_gemv_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    q4k_gemv_kernel<M><<<static_cast<unsigned>(p.n / kRows), kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
+    if (p.m <= 1) return launch_gemv_m<1>(p, s);
+    if (p.m <= 2) return launch_gemv_m<2>(p, s);
+    if (p.m <= 4) return launch_gemv_m<4>(p, s);
+    if (p.m <= 8) return launch_gemv_m<8>(p, s);
+    return launch_gemv_m<16>(p, s);
+}
+
+}  // namespace q4k

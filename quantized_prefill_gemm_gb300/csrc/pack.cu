@@ -10,8 +10,10 @@
 //
 // Output (q4k_layout.h): per (128-row tile, chunk) records of 16 B of quants
 // in the order the GEMM's converter expands them, the sc bytes, the fp32 d of
-// each super-block, and -(dmin*m) split into two bf16 planes for the min-term
-// GEMM.  One thread per (od row, super-block); runs once per weight matrix.
+// each super-block, -(dmin*m) split into two bf16 planes for the min-term
+// GEMM, and for the small-M path the m bytes and the fp32 dmin of each
+// super-block.  One thread per (od row, super-block); runs once per weight
+// matrix.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -25,7 +27,8 @@ constexpr int kThreadsPerBlock = 128;
 
 __global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* __restrict__ blocks, int64_t n,
                                                                 int64_t k, uint8_t* __restrict__ packed,
-                                                                int64_t off_sc, int64_t off_dsb, int64_t off_ndm) {
+                                                                int64_t off_sc, int64_t off_dsb, int64_t off_ndm,
+                                                                int64_t off_mq, int64_t off_dmn) {
     const int64_t ksb = k / 256, kc = k / 32;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= n * ksb) return;
@@ -57,6 +60,8 @@ __global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* _
     uint8_t* scp = packed + off_sc;
     float* dsb = reinterpret_cast<float*>(packed + off_dsb);
     __nv_bfloat16* ndm = reinterpret_cast<__nv_bfloat16*>(packed + off_ndm);
+    uint8_t* mqp = packed + off_mq;
+    float* dmn = reinterpret_cast<float*>(packed + off_dmn);
 
     for (int j = 0; j < 8; ++j) {   // sub-block = chunk c of this super-block
         const int64_t c = sb * 8 + j;
@@ -78,6 +83,7 @@ __global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* _
         const int64_t rec = (nt * kc + c) * 128 + r;
         *reinterpret_cast<uint4*>(nib + rec * 16) = make_uint4(words[0], words[1], words[2], words[3]);
         scp[rec] = static_cast<uint8_t>(scv[j]);
+        mqp[rec] = static_cast<uint8_t>(mv[j]);
         const float v = -(dmin * static_cast<float>(mv[j]));   // exact: 11-bit x 6-bit
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -85,6 +91,7 @@ __global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* _
         ndm[(n + o) * kc + c] = lo;
     }
     dsb[(nt * ksb + sb) * 128 + r] = d;
+    dmn[(nt * ksb + sb) * 128 + r] = dmin;
 }
 
 }  // namespace
@@ -94,7 +101,7 @@ cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* pa
     const int64_t threads = n * (k / 256);
     if (threads == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((threads + kThreadsPerBlock - 1) / kThreadsPerBlock);
-    pack_kernel<<<grid, kThreadsPerBlock, 0, s>>>(blocks, n, k, packed, L.sc, L.dsb, L.ndm);
+    pack_kernel<<<grid, kThreadsPerBlock, 0, s>>>(blocks, n, k, packed, L.sc, L.dsb, L.ndm, L.mq, L.dmn);
     return cudaGetLastError();
 }
 

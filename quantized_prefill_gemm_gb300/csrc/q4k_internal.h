@@ -23,6 +23,24 @@ struct GemmParams {
     int out_bf16;
 };
 
+// Small-M product (gemv.cu): packed weights as for the GEMM, activations as
+// the q8 SoA of q8_quantize_rows (q8 rows, d_a and ssum 16-byte aligned,
+// ldq % 16 == 0).
+struct GemvParams {
+    const uint8_t* nib;      // packed quants  [nt][kc][128][16 B]
+    const uint8_t* sc;       // packed scales  [nt][kc][128]
+    const uint8_t* mq;       // packed mins    [nt][kc][128]
+    const float* dsb;        // super-block d    [nt][ksb][128]
+    const float* dmn;        // super-block dmin [nt][ksb][128]
+    const int8_t* q8;        // [m][ldq]
+    const uint16_t* da;      // f16 bits [m][kc]
+    const int16_t* ssum;     // [m][kc]
+    void* y;                 // [m][ldy]
+    int64_t ldq, ldy;
+    int m, n, k, kc, ksb;
+    int out_bf16;
+};
+
 cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8,
                                     uint16_t* da, int16_t* ssum, cudaStream_t s);
 cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s);
@@ -31,6 +49,7 @@ cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16
 cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                         const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s);
 
 }  // namespace q4k

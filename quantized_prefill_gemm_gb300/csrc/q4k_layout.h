@@ -12,6 +12,8 @@
 //   dsb  [nt][ksb][128] f32   super-block scale d
 //   ndm  [2][n][kc]     bf16  -(dmin*m) split into hi = bf16(v) (plane 0) and
 //                              lo = bf16(v - hi) (plane 1)
+//   mq   [nt][kc][128]  u8    6-bit sub-block min m        (small-M path)
+//   dmn  [nt][ksb][128] f32   super-block dmin             (small-M path)
 //
 // Activation workspace (q4k_act_quantize / q4k_act_from_q8 -> q4k_gemm), for m
 // tokens, mp = m rounded up to 128:
@@ -32,14 +34,16 @@ constexpr int64_t kTileN = 128;   // output features per GEMM tile
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 struct PackedLayout {
-    int64_t nib, sc, dsb, ndm, total;
+    int64_t nib, sc, dsb, ndm, mq, dmn, total;
     PackedLayout(int64_t n, int64_t k) {
         const int64_t kc = k / 32, ksb = k / 256;
         nib = 0;
         sc = align_up(nib + n * k / 2, kAlign);
         dsb = align_up(sc + n * kc, kAlign);
         ndm = align_up(dsb + n * ksb * 4, kAlign);
-        total = align_up(ndm + 2 * n * kc * 2, kAlign);
+        mq = align_up(ndm + 2 * n * kc * 2, kAlign);
+        dmn = align_up(mq + n * kc, kAlign);
+        total = align_up(dmn + n * ksb * 4, kAlign);
     }
 };
 

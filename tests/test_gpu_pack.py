@@ -45,3 +45,11 @@ def test_pack_layout_round_trip(n, k, seed):
     want = -np.repeat(q4k_blocks.f16_bits_to_f64(f["dmin_bits"]), 8, axis=1) * f["m"].astype(np.float64)
     got = _bf16(ndm[0]) + _bf16(ndm[1])
     assert np.all(np.abs(got - want) <= 2.0 ** -16 * np.abs(want))
+    # small-M sections: the 6-bit m per (row, chunk) and the fp32 dmin per (row, super-block)
+    off_mq = align(off_ndm + 4 * n * kc)
+    off_dmn = align(off_mq + n * kc)
+    mq = pk[off_mq: off_mq + n * kc].reshape(nt, kc, 128).transpose(0, 2, 1).reshape(n, kc)
+    assert np.array_equal(mq, f["m"])
+    dmn = pk[off_dmn: off_dmn + n * ksb * 4].view(np.float32).reshape(nt, ksb, 128).transpose(0, 2, 1).reshape(n, ksb)
+    assert np.array_equal(dmn.astype(np.float64), q4k_blocks.f16_bits_to_f64(f["dmin_bits"]))
+    assert packed.numel() == align(off_dmn + n * ksb * 4)
