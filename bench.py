@@ -6,6 +6,10 @@ tokens, a distinct fp32 activation matrix per projection (224 buffers), fused
 q8 activation quantization, bf16 output.  One step = all 224 projections
 (activation quantization + GEMM each).  tok/s = 2048 / step time.
 
+--workload decode runs the same 224 projections for one token (the small-M
+path, bound by reading 3.64 GB of packed weights), captured in a CUDA graph
+so that the timed region holds no host launch overhead.
+
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
 Multi-GPU (torchrun): every rank runs its own replica of the workload (no data
 exchange); value = all ranks' tokens / max step time over ranks.
@@ -37,6 +41,10 @@ WORKLOADS = {
             "7B FFN linears gate/up 11008x4096 + down 4096x11008 Q4_K, 2048 tokens, fused q8, bf16 out"),
     "qproj2630": (2630, [(4096, 4096)], "bf16", "7B q-proj 4096x4096 Q4_K, 2630 tokens (outlier channels), fused q8, bf16 out"),
     "qproj512": (512, [(4096, 4096)], "f32", "7B q-proj 4096x4096 Q4_K, 512 tokens, fused q8, fp32 out"),
+    "decode": (1, [(n, k) for _ in range(32) for (_, n, k) in LAYER], "bf16",
+               "7B linear stack at decode size: 32 layers x {q,k,v,o 4096x4096; gate,up 11008x4096; down "
+               "4096x11008} Q4_K, 1 token, fused q8 activation quantization, bf16 out (small-M path, "
+               "CUDA-graph replay)"),
 }
 
 
@@ -176,6 +184,8 @@ def main():
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
+    if args.workload == "decode":
+        return run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream)
 
     def step(events=None):
         for i, (n, k) in enumerate(mats):
@@ -283,6 +293,102 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2)
     d2h = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
     return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps}
+
+
+def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream):
+    """One token through all 224 projections, replayed from a CUDA graph.
+
+    value: tok/s of the fused step (q8 quantization + small-M product per
+    projection).  roofline: the small-M kernel alone (a second graph of the
+    224 products on pre-quantized activations), algorithmic bytes = packed
+    Q4_K weights at 144 B / 256 + the q8 input (1 B per element + 4 B per 32)
+    + the bf16 output, against the measured HBM copy bandwidth."""
+    tokens, out = 1, "bf16"
+    q8s = [q4k.q8_quantize_rows(x) for x in xs]
+
+    def fused():
+        for i, (n, k) in enumerate(mats):
+            q4k.q4k_gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws)
+
+    def products():
+        for i, (n, k) in enumerate(mats):
+            q, da, ss = q8s[i]
+            q4k.q4k_gemm(packed[i], n, k, q, out_dtype=out, da=da, ssum=ss, y=ys[i], workspace=ws)
+
+    side = torch.cuda.Stream(device=dev)
+    graphs = {}
+    with torch.cuda.stream(side):
+        for _ in range(args.warmup):
+            fused()
+            products()
+    torch.cuda.synchronize()
+    for name, fn in (("fused", fused), ("products", products)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        graphs[name] = g
+    for _ in range(args.warmup):
+        graphs["fused"].replay()
+        graphs["products"].replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    def timed(g, reps):   # replays run on the current stream; the events bracket them there
+        cur = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(cur)
+        for _ in range(reps):
+            g.replay()
+        b.record(cur)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    clocks = ClockSampler(local)
+    torch.cuda.nvtx.range_push("timed")
+    ms_step = timed(graphs["fused"], args.steps)
+    torch.cuda.nvtx.range_pop()
+    clk = clocks.stop()
+    ms_products = timed(graphs["products"], args.steps)
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+        dist.barrier()
+    err = q4k.q4k_device_error_word()
+    if err:
+        raise RuntimeError(f"device error word 0x{err:x}")
+
+    bytes_step = sum(n * k * 144 / 256 + tokens * (k + k // 32 * 4) + tokens * n * 2 for n, k in mats)
+    peaks, src = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = bytes_step / (ms_products * 1e-3) / 1e9
+    flops_step = sum(2.0 * tokens * n * k for n, k in mats)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "q4k_gemv_kernel",
+                "peak_source": f"{src} HBM copy bandwidth",
+                "per_launch": "algorithmic bytes (Q4_K weights 144 B/256 + q8 input + bf16 output) / "
+                              "graph-replayed duration of the 224 small-M products, per launch"}
+    desc = WORKLOADS[args.workload][3]
+    line = {"metric": METRIC, "value": world * tokens / (ms_step * 1e-3), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a on exact q4/q8 integers, fp32 rescale",
+            "data": "synthetic (seeded random Q4_K weights and activations)",
+            "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
+                       "l2": "inputs larger than L2 (3.64 GB of weights per step)",
+                       "parallelism": f"replicas x{world}"},
+            "effective_tops": world * flops_step / (ms_step * 1e-3) / 1e12,
+            "products_ms_per_step": ms_products, "roofline": roofline, "clocks": clk,
+            "gpu_launches": 2 * len(mats) * args.steps}
+    if not args.no_e2e and rank == 0:
+        line["e2e"] = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"], _ = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
