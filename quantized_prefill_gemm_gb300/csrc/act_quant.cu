@@ -17,6 +17,7 @@
 
 #include "q4k_internal.h"
 #include "q4k_layout.h"
+#include "q4k_ptx.cuh"
 
 namespace q4k {
 namespace {
@@ -69,6 +70,11 @@ __global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_kernel(const float* 
                                                                    int64_t ldx, int8_t* __restrict__ q8,
                                                                    uint16_t* __restrict__ da,
                                                                    int16_t* __restrict__ ssum) {
+    // launched with programmatic dependent launch: let the next kernel (the
+    // small-M product) start staging its weights, and wait for the previous
+    // one (which may still read q8/da/ssum, or have written x) to finish
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t kc = k / 32;
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t grp = gid >> 3;
@@ -170,8 +176,16 @@ cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_
                                     int16_t* ssum, cudaStream_t s) {
     const int64_t threads = m * (k / 32) * 8;
     if (threads == 0) return cudaSuccess;
-    q8_rows_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(x, m, k, ldx, q8, da, ssum);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_for(threads));
+    cfg.blockDim = dim3(kThreadsPerBlock);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, q8_rows_kernel, x, m, k, ldx, q8, da, ssum);
 }
 
 cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s) {

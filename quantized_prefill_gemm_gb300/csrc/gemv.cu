@@ -15,7 +15,9 @@
 // token) into its own shared-memory stage with 16-B loads, while the quants
 // of the next super-block are already on their way into registers; all 16
 // lanes then read the stage (broadcast).  The 16 partial sums of a row are
-// added in shared memory in a fixed order (deterministic), then stored.
+// added in shared memory in a fixed order (deterministic), then stored.  The
+// kernel is launched with programmatic dependent launch, so that its quants
+// stream into L2 while the kernel before it finishes.
 //
 // Per thread and chunk: J[t] = sum_{k in chunk} q[k] * qa[t][k] (exact,
 // dp4a), P[t] += d_a[t] * (sc * J[t]) (sc*J < 2^22 is exact in fp32),
@@ -25,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "q4k_internal.h"
+#include "q4k_ptx.cuh"
 
 namespace q4k {
 namespace {
@@ -86,6 +89,19 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const GemvParams p) 
     const int64_t nt = o >> 7, r = o & 127;
     const int kc = p.kc, ksb = p.ksb, m = p.m;
     Stage<M>& st = stages[part];
+
+    // Launched with programmatic dependent launch: while the previous kernel
+    // in the stream (normally the activation quantization) still runs, pull
+    // this CTA's quants (16 rows x 16 B per chunk, 256 contiguous bytes) from
+    // HBM into L2, then wait for that kernel before reading activations.
+    griddep_launch_dependents();
+    {
+        const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRows;
+        const int64_t tile0 = row0 >> 7, r0 = row0 & 127;
+        for (int c = threadIdx.x; c < kc; c += kThreads)
+            prefetch_l2(p.nib + ((tile0 * kc + c) * 128 + r0) * 16, kRows * 16);
+    }
+    griddep_wait();
 
     float acc[M];
 #pragma unroll
@@ -193,8 +209,17 @@ cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    q4k_gemv_kernel<M><<<static_cast<unsigned>(p.n / kRows), kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n / kRows));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<M>, p);
 }
 
 }  // namespace

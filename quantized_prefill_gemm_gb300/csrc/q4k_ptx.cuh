@@ -95,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Same, ignoring the abort flag (teardown: wait for own copies in flight).
-__device__ __noinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t timeout) {
+static __device__ __noinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t timeout) {
     const long long t0 = clock64();
     while (!mbar_try_wait_sleep(bar, parity)) {
         if (static_cast<uint64_t>(clock64() - t0) > timeout) return false;
@@ -267,6 +267,24 @@ __device__ __forceinline__ uint64_t ffma2_pk(uint64_t a, uint64_t b, uint64_t c)
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
+}
+
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start while the previous kernel in the
+// stream is still running: griddep_wait() blocks until that kernel has
+// finished and its memory is visible (it returns at once for a kernel
+// launched without the attribute), griddep_launch_dependents() lets the next
+// such kernel start early.  Nothing written by the previous kernel may be read
+// (or anything it reads be written) before griddep_wait().
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Bring `bytes` (a multiple of 16, 16-byte aligned address) into L2.  Only a
+// hint: it cannot change what a later load returns.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
 }
 
 }  // namespace q4k
