@@ -45,6 +45,9 @@ WORKLOADS = {
                "7B linear stack at decode size: 32 layers x {q,k,v,o 4096x4096; gate,up 11008x4096; down "
                "4096x11008} Q4_K, 1 token, fused q8 activation quantization, bf16 out (small-M path, "
                "CUDA-graph replay)"),
+    "decode_gate": (1, [(11008, 4096)], "bf16",
+                    "7B FFN gate projection 11008x4096 Q4_K at decode size: 1 token, fused q8, bf16 out "
+                    "(small-M path, CUDA-graph replay)"),
 }
 
 
@@ -184,7 +187,7 @@ def main():
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
-    if args.workload == "decode":
+    if tokens <= 16:   # decode-sized: the small-M path
         return run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream)
 
     def step(events=None):
@@ -296,14 +299,15 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2)
 
 
 def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream):
-    """One token through all 224 projections, replayed from a CUDA graph.
+    """Decode-sized workloads (tokens <= 16): one step through all the
+    workload's projections, replayed from a CUDA graph.
 
     value: tok/s of the fused step (q8 quantization + small-M product per
     projection).  roofline: the small-M kernel alone (a second graph of the
     224 products on pre-quantized activations), algorithmic bytes = packed
     Q4_K weights at 144 B / 256 + the q8 input (1 B per element + 4 B per 32)
     + the bf16 output, against the measured HBM copy bandwidth."""
-    tokens, out = 1, "bf16"
+    tokens, out = WORKLOADS[args.workload][0], WORKLOADS[args.workload][2]
     q8s = [q4k.q8_quantize_rows(x) for x in xs]
 
     def fused():
@@ -361,6 +365,7 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
         raise RuntimeError(f"device error word 0x{err:x}")
 
     bytes_step = sum(n * k * 144 / 256 + tokens * (k + k // 32 * 4) + tokens * n * 2 for n, k in mats)
+    weights_gb = sum(n * k * 144 / 256 for n, k in mats) / 1e9
     peaks, src = load_peaks()
     peak = float(peaks["hbm_gbs"])
     achieved = bytes_step / (ms_products * 1e-3) / 1e9
@@ -376,7 +381,8 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
             "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a on exact q4/q8 integers, fp32 rescale",
             "data": "synthetic (seeded random Q4_K weights and activations)",
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
-                       "l2": "inputs larger than L2 (3.64 GB of weights per step)",
+                       "l2": f"{weights_gb:.2f} GB of weights per step" + (
+                           " (larger than L2)" if weights_gb > 0.2 else " (L2-resident between replays)"),
                        "parallelism": f"replicas x{world}"},
             "effective_tops": world * flops_step / (ms_step * 1e-3) / 1e12,
             "products_ms_per_step": ms_products, "roofline": roofline, "clocks": clk,
