@@ -302,8 +302,8 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
     """Decode-sized workloads (tokens <= 16): one step through all the
     workload's projections, replayed from a CUDA graph.
 
-    value: tok/s of the fused step (q8 quantization + small-M product per
-    projection).  roofline: the small-M kernel alone (a second graph of the
+    value: tok/s of the fused step (one small-M launch per projection, which
+    quantizes the fp32 activations in the kernel).  roofline: the small-M kernel alone (a second graph of the
     224 products on pre-quantized activations), algorithmic bytes = packed
     Q4_K weights at 144 B / 256 + the q8 input (1 B per element + 4 B per 32)
     + the bf16 output, against the measured HBM copy bandwidth."""
@@ -386,7 +386,7 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
                        "parallelism": f"replicas x{world}"},
             "effective_tops": world * flops_step / (ms_step * 1e-3) / 1e12,
             "products_ms_per_step": ms_products, "roofline": roofline, "clocks": clk,
-            "gpu_launches": 2 * len(mats) * args.steps}
+            "gpu_launches": (1 if tokens <= 4 else 2) * len(mats) * args.steps}
     if not args.no_e2e and rank == 0:
         line["e2e"] = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
     if rank == 0 and not args.no_cpu_baseline:

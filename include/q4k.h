@@ -119,12 +119,16 @@ q4k_status q4k_pack_weights(const void* q4k_blocks, int64_t n, int64_t k,
  * output) where a = d_a*qa, and the per-chunk integer dot products are exact.
  * Small M: for 1 <= m <= Q4K_SMALL_M tokens (decode-sized batches) the call
  * runs a CUDA-core kernel whose cost is reading the packed weights (integer
- * dot products with dp4a, same rescale and accuracy contract); the f32 path
- * then uses the first bytes of `workspace` for the q8 SoA, and the q8 path
- * reads the caller's arrays directly when q8, da_f16 and ssum are 16-byte
- * aligned and ldx % 16 == 0 (otherwise it takes the general path).
+ * dot products with dp4a, same rescale and accuracy contract).  With f32
+ * input and m <= Q4K_FUSED_QUANT_M it is one launch that quantizes the
+ * activations inside the kernel (the same q8, d_a and ssum bits as
+ * q8_quantize_rows) and leaves `workspace` untouched (it may then be NULL);
+ * for larger m the q8 SoA is first written to the start of `workspace`.  The
+ * q8 path reads the caller's arrays directly when q8, da_f16 and ssum are
+ * 16-byte aligned and ldx % 16 == 0 (otherwise it takes the general path).
  * ------------------------------------------------------------------------ */
 #define Q4K_SMALL_M 16
+#define Q4K_FUSED_QUANT_M 4
 size_t q4k_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int act);
 q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k,
                     int act, const void* x_or_q8, const void* da_f16, const void* ssum,

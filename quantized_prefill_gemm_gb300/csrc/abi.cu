@@ -182,10 +182,12 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
     return from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream));
 }
 
-// Small-M path: the q8 SoA (q8 rows, d_a and ssum 16-byte aligned, ldq % 16 ==
-// 0) times the packed weights on the CUDA cores.
+// Small-M path on the CUDA cores: the packed weights times either the q8 SoA
+// (q8 rows, d_a and ssum 16-byte aligned, ldq % 16 == 0) or, when xf is set,
+// fp32 activations (16-byte aligned, ldx % 4 == 0) quantized in the kernel.
 q4k_status run_gemv(const void* packed_w, int64_t n, int64_t k, const int8_t* q8, const uint16_t* da,
-                    const int16_t* ssum, int64_t m, int64_t ldq, void* y, int out, int64_t ldy, cudaStream_t stream) {
+                    const int16_t* ssum, const float* xf, int64_t m, int64_t ldq, void* y, int out, int64_t ldy,
+                    cudaStream_t stream) {
     DeviceInfo* dev = nullptr;
     q4k_status st = device_info(&dev);
     if (st != Q4K_OK) return st;
@@ -201,8 +203,10 @@ q4k_status run_gemv(const void* packed_w, int64_t n, int64_t k, const int8_t* q8
     g.q8 = q8;
     g.da = da;
     g.ssum = ssum;
+    g.xf = xf;
     g.y = y;
-    g.ldq = ldq;
+    g.ldq = xf ? 0 : ldq;
+    g.ldx = xf ? ldq : 0;
     g.ldy = ldy;
     g.m = static_cast<int>(m);
     g.n = static_cast<int>(n);
@@ -213,7 +217,8 @@ q4k_status run_gemv(const void* packed_w, int64_t n, int64_t k, const int8_t* q8
     return from_cuda(launch_gemv(g, stream));
 }
 
-// Where the small-M path keeps the q8 SoA inside a q4k_gemm workspace.
+// Where the small-M path keeps the q8 SoA inside a q4k_gemm workspace (token
+// counts above kFusedQuantMaxM).
 struct SmallMLayout {
     int64_t q8, da, ssum, total;
     SmallMLayout(int64_t m, int64_t k) {
@@ -224,6 +229,11 @@ struct SmallMLayout {
         total = align_up(ssum + m * kc * 2, 256);
     }
 };
+
+// Up to this many tokens the small-M kernel quantizes fp32 activations itself.
+// Every CTA quantizes the whole activation block it reads, so the repeated
+// work grows with m; beyond 4 tokens a separate q8 pass is faster.
+constexpr int64_t kFusedQuantMaxM = Q4K_FUSED_QUANT_M;
 
 }  // namespace
 }  // namespace q4k
@@ -333,7 +343,10 @@ q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
     if (!aligned(packed_w, 256)) return Q4K_ERR_ALIGNMENT;
     if (m >= 1 && m <= Q4K_SMALL_M) {   // decode-sized: CUDA-core path, bound by the weight stream
         if (act == Q4K_ACT_F32) {
-            if ((st = check_act_f32(static_cast<const float*>(x_or_q8), m, k, ldx)) != Q4K_OK) return st;
+            const float* xf = static_cast<const float*>(x_or_q8);
+            if ((st = check_act_f32(xf, m, k, ldx)) != Q4K_OK) return st;
+            if (m <= kFusedQuantMaxM)   // one launch: the kernel quantizes the activations itself
+                return run_gemv(packed_w, n, k, nullptr, nullptr, nullptr, xf, m, ldx, y, out_dtype, ldy, stream);
             const SmallMLayout L(m, k);
             if (!workspace) return Q4K_ERR_INVALID_ARG;
             if (!aligned(workspace, 256)) return Q4K_ERR_ALIGNMENT;
@@ -342,16 +355,16 @@ q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
             int8_t* q8 = reinterpret_cast<int8_t*>(wsb + L.q8);
             uint16_t* da = reinterpret_cast<uint16_t*>(wsb + L.da);
             int16_t* ss = reinterpret_cast<int16_t*>(wsb + L.ssum);
-            st = q8_quantize_rows(static_cast<const float*>(x_or_q8), m, k, ldx, q8, da, ss, stream);
+            st = q8_quantize_rows(xf, m, k, ldx, q8, da, ss, stream);
             if (st != Q4K_OK) return st;
-            return run_gemv(packed_w, n, k, q8, da, ss, m, k, y, out_dtype, ldy, stream);
+            return run_gemv(packed_w, n, k, q8, da, ss, nullptr, m, k, y, out_dtype, ldy, stream);
         }
         const int8_t* q8 = static_cast<const int8_t*>(x_or_q8);
         if (!q8 || !da_f16 || !ssum) return Q4K_ERR_INVALID_ARG;
         if (ldx < k) return Q4K_ERR_SHAPE;
         if (aligned(q8, 16) && ldx % 16 == 0 && aligned(da_f16, 16) && aligned(ssum, 16))
             return run_gemv(packed_w, n, k, q8, static_cast<const uint16_t*>(da_f16),
-                            static_cast<const int16_t*>(ssum), m, ldx, y, out_dtype, ldy, stream);
+                            static_cast<const int16_t*>(ssum), nullptr, m, ldx, y, out_dtype, ldy, stream);
         // other alignments go through the general path below
     }
     if (act == Q4K_ACT_F32) {

@@ -19,6 +19,14 @@
 // kernel is launched with programmatic dependent launch, so that its quants
 // stream into L2 while the kernel before it finishes.
 //
+// With fp32 activations (kQuant, up to 4 tokens) the stage is filled by
+// quantizing them in place of the copy: every CTA quantizes the activations of the super-blocks
+// it reads, exactly as the stand-alone q8 quantizer does (same fp32
+// operations, so the same q8, d_a and ssum bits), which saves that kernel's
+// launch and its round trip through HBM.  The fp32 rows are re-read by every
+// CTA from L2 (4 B per element instead of 1), a small cost next to the weights
+// at decode sizes.
+//
 // Per thread and chunk: J[t] = sum_{k in chunk} q[k] * qa[t][k] (exact,
 // dp4a), P[t] += d_a[t] * (sc * J[t]) (sc*J < 2^22 is exact in fp32),
 // Z[t] += (d_a[t] * ssum[t]) * (-dmin * m) (both factors exact in fp32); per
@@ -78,8 +86,54 @@ __device__ __forceinline__ void load_weights(const GemvParams& p, int64_t nt, in
     }
 }
 
+// Quantize one token's 256 activations of a super-block into the stage.  Lane
+// hl of the half-warp takes k = 16 hl .. 16 hl + 15, half of chunk hl / 2; the
+// chunk's amax and ssum are completed with the partner lane hl ^ 1.  Rounding
+// as in the stand-alone quantizer ("34 · r31 — q-major sda scale-read
+// repack", §1 gives the block format; the order is ours): d = RN32(amax/127),
+// inv = RN32(127/amax), qa = clamp(rint_even(RN32(x*inv)), -127, 127),
+// d_a = RN16(d), and a block with amax < 2^-120 is a zero block.
 template <int M>
-__global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const GemvParams p) {
+__device__ __forceinline__ void quantize_to_stage(const float* __restrict__ x, unsigned hmask, int hl, int t,
+                                                  Stage<M>& st) {
+    const float4* src = reinterpret_cast<const float4*>(x) + 4 * hl;
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 f = __ldg(src + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    float amax = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, 1));
+    const bool live = amax >= 0x1p-120f;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __fdiv_rn(127.0f, amax);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        int q = __float2int_rn(__fmul_rn(v[i], inv));
+        q = max(-127, min(127, q));
+        q = live ? q : 0;
+        s += q;
+        w[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
+    }
+    s += __shfl_xor_sync(hmask, s, 1);
+    st.qa[t][hl] = make_int4(static_cast<int>(w[0]), static_cast<int>(w[1]), static_cast<int>(w[2]),
+                             static_cast<int>(w[3]));
+    if ((hl & 1) == 0) {
+        reinterpret_cast<uint16_t*>(&st.da[t])[hl >> 1] = __half_as_ushort(__float2half_rn(live ? d : 0.0f));
+        reinterpret_cast<int16_t*>(&st.ss[t])[hl >> 1] = static_cast<int16_t>(s);
+    }
+}
+
+template <int M, bool kQuant>
+__global__ void __launch_bounds__(kThreads, kQuant ? 2 : 1) q4k_gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Stage<M>* stages = reinterpret_cast<Stage<M>*>(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -123,14 +177,23 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const GemvParams p) 
             continue;
         }
         // stage this super-block's activations (the half-warp shares them)
+        if constexpr (kQuant) {
+            // the next weights are requested first: the quantization waits on its loads
+            if (sb + kParts < ksb) load_weights(p, nt, r, sb + kParts, nxt);
+            const unsigned hmask = 0xFFFFu << (lane & 16);
+#pragma unroll 2
+            for (int t = 0; t < M; ++t)
+                if (t < m) quantize_to_stage<M>(p.xf + t * p.ldx + 256 * sb, hmask, hl, t, st);
+        } else {
 #pragma unroll
-        for (int t = 0; t < M; ++t)
-            if (t < m) st.qa[t][hl] = __ldg(reinterpret_cast<const int4*>(p.q8 + t * p.ldq + 256 * sb) + hl);
-        if (hl < m && hl < M) {
-            st.da[hl] = __ldg(reinterpret_cast<const uint4*>(p.da + hl * kc + 8 * sb));
-            st.ss[hl] = __ldg(reinterpret_cast<const uint4*>(p.ssum + hl * kc + 8 * sb));
+            for (int t = 0; t < M; ++t)
+                if (t < m) st.qa[t][hl] = __ldg(reinterpret_cast<const int4*>(p.q8 + t * p.ldq + 256 * sb) + hl);
+            if (hl < m && hl < M) {
+                st.da[hl] = __ldg(reinterpret_cast<const uint4*>(p.da + hl * kc + 8 * sb));
+                st.ss[hl] = __ldg(reinterpret_cast<const uint4*>(p.ssum + hl * kc + 8 * sb));
+            }
+            if (sb + kParts < ksb) load_weights(p, nt, r, sb + kParts, nxt);   // in flight during this one
         }
-        if (sb + kParts < ksb) load_weights(p, nt, r, sb + kParts, nxt);   // in flight during this one
         const int64_t srec = (nt * ksb + sb) * 128 + r;
         const float d = __ldg(p.dsb + srec);
         const float dmin = __ldg(p.dmn + srec);
@@ -196,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const GemvParams p) 
     }
 }
 
-template <int M>
+template <int M, bool kQuant>
 cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -205,7 +268,7 @@ cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     constexpr size_t smem = gemv_smem_bytes<M>();
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(q4k_gemv_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        e = cudaFuncSetAttribute(q4k_gemv_kernel<M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -219,17 +282,26 @@ cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<M>, p);
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<M, kQuant>, p);
+}
+
+cudaError_t launch_gemv_q8(const GemvParams& p, cudaStream_t s) {
+    if (p.m <= 1) return launch_gemv_m<1, false>(p, s);
+    if (p.m <= 2) return launch_gemv_m<2, false>(p, s);
+    if (p.m <= 4) return launch_gemv_m<4, false>(p, s);
+    if (p.m <= 8) return launch_gemv_m<8, false>(p, s);
+    return launch_gemv_m<16, false>(p, s);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
-    if (p.m <= 1) return launch_gemv_m<1>(p, s);
-    if (p.m <= 2) return launch_gemv_m<2>(p, s);
-    if (p.m <= 4) return launch_gemv_m<4>(p, s);
-    if (p.m <= 8) return launch_gemv_m<8>(p, s);
-    return launch_gemv_m<16>(p, s);
+    if (!p.xf) return launch_gemv_q8(p, s);
+    // in-kernel quantization is built for up to 4 tokens (the caller's limit)
+    if (p.m <= 1) return launch_gemv_m<1, true>(p, s);
+    if (p.m <= 2) return launch_gemv_m<2, true>(p, s);
+    if (p.m <= 4) return launch_gemv_m<4, true>(p, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace q4k

@@ -35,8 +35,9 @@ struct GemvParams {
     const int8_t* q8;        // [m][ldq]
     const uint16_t* da;      // f16 bits [m][kc]
     const int16_t* ssum;     // [m][kc]
+    const float* xf;         // fp32 activations [m][ldx]; when set, quantized in the kernel (q8/da/ssum unused)
     void* y;                 // [m][ldy]
-    int64_t ldq, ldy;
+    int64_t ldq, ldx, ldy;
     int m, n, k, kc, ksb;
     int out_bf16;
 };

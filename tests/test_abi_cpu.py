@@ -91,7 +91,8 @@ def test_host_validation_rejects_before_any_cuda_call(q4k):
     assert gemm(ldy=100) == 2
     assert gemm(ldy=258) == 3            # fp32 rows must stay 16-byte aligned
     assert gemm(ldx=500) == 2
-    assert gemm(ws_bytes=16) == 4
+    assert gemm(m=32, ws_bytes=16) == 4   # general path (m > 16); the small-M fp32 path takes no workspace
+    assert gemm(m=32, act=1, ws_bytes=16) == 1
     assert gemm(act=1) == 1              # q8 input without da / ssum
     assert gemm(m=0) == 0                # empty batch is a no-op
     # debug hook size limit

@@ -86,3 +86,73 @@ def test_matches_general_path_and_repeats(q4k):
     assert torch.equal(y1, y2)
     _, scale = oracle_rows(blocks, x, np.arange(m))
     assert_close(y1.cpu().double().numpy(), yg.cpu().double().numpy(), scale, "f32", "small-M vs GEMM")
+
+
+def _special_blocks(x):
+    """Overwrite some 32-element blocks with the quantizer's special cases:
+    all zero, below the 2^-120 zero-block threshold, subnormal, a single
+    non-zero element, an amax just above the threshold, halves that round to
+    even (x * 127 / amax = j + 0.5), and all-negative."""
+    x = x.copy()
+    m, k = x.shape
+    kc = k // 32
+    for t in range(m):
+        c = (3 * t) % kc
+        x[t, 32 * c:32 * c + 32] = 0.0
+        c = (3 * t + 1) % kc
+        x[t, 32 * c:32 * c + 32] = np.float32(1e-37) * np.sign(x[t, 32 * c:32 * c + 32])
+        c = (3 * t + 2) % kc
+        x[t, 32 * c:32 * c + 32] = np.float32(1e-40)
+        c = (13 * t + 17) % kc
+        x[t, 32 * c:32 * c + 32] *= np.float32(2e-36) / np.abs(x[t, 32 * c:32 * c + 32]).max()   # just live
+        c = (5 * t + 7) % kc
+        x[t, 32 * c:32 * c + 32] = 0.0
+        x[t, 32 * c + 5] = -3.0
+        c = (7 * t + 11) % kc
+        x[t, 32 * c:32 * c + 32] = (np.arange(32, dtype=np.float32) + 0.5) * np.float32(1.0 / 127.0)
+        x[t, 32 * c + 31] = 1.0   # amax 1: x * 127 = j + 0.5 for the other 31
+        c = (11 * t + 13) % kc
+        x[t, 32 * c:32 * c + 32] = -np.abs(x[t, 32 * c:32 * c + 32]) - np.float32(0.25)
+    return x
+
+
+@pytest.mark.parametrize("n,k,m,kind", [(256, 512, 1, "normal"), (384, 768, 3, "outlier"),
+                                        (512, 11008, 4, "silu_mul"), (256, 4096, 2, "special"),
+                                        (256, 4096, 4, "special"), (128, 2816, 1, "special")])
+def test_in_kernel_quantization_matches_prepass_bits(q4k, n, k, m, kind):
+    """fp32 activations (up to 4 tokens) are quantized inside the small-M kernel.  The q8, d_a
+    and ssum it stages must be the stand-alone quantizer's bit for bit, so the
+    output equals, bit for bit, the same kernel fed the quantizer's arrays;
+    both are also checked against the oracle."""
+    blocks, x = make_case(n, k, m, "normal" if kind == "special" else kind, 80 + m)
+    if kind == "special":
+        x = _special_blocks(x)
+    packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+    xd = to_dev(x)
+    y_fused = q4k.q4k_gemm(packed, n, k, xd, out_dtype="f32")
+    q, da, ss = q4k.q8_quantize_rows(xd)
+    y_pre = q4k.q4k_gemm(packed, n, k, q, out_dtype="f32", da=da, ssum=ss)
+    torch.cuda.synchronize()
+    assert torch.equal(y_fused, y_pre)
+    want, scale = oracle_rows(blocks, x, np.arange(m))
+    assert_close(y_fused.cpu().double().numpy(), want, scale, "f32", f"in-kernel quantization {kind}")
+
+
+def test_in_kernel_quantization_strided_rows_and_no_workspace(q4k):
+    """Row stride ldx > k, and the fp32 small-M call made with a NULL
+    workspace (it does not use one)."""
+    import ctypes
+
+    n, k, m = 256, 1024, 3
+    blocks, x = make_case(n, k, m, "outlier", 90)
+    packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+    xw = torch.zeros((m, k + 12), dtype=torch.float32, device=DEV)
+    xw[:, :k] = to_dev(x)
+    y = torch.full((m, n), float("nan"), dtype=torch.float32, device=DEV)
+    st = q4k.LIB.q4k_gemm(ctypes.c_void_p(packed.data_ptr()), n, k, q4k.ACT_F32, ctypes.c_void_p(xw.data_ptr()),
+                          None, None, m, k + 12, ctypes.c_void_p(y.data_ptr()), 0, n, None, 0,
+                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, q4k.LIB.q4k_status_string(st)
+    torch.cuda.synchronize()
+    want, scale = oracle_rows(blocks, x, np.arange(m))
+    assert_close(y.cpu().double().numpy(), want, scale, "f32", "strided fp32 rows, no workspace")
