@@ -6,6 +6,11 @@ tokens, a distinct fp32 activation matrix per projection (224 buffers), fused
 q8 activation quantization, bf16 output.  One step = all 224 projections
 (activation quantization + GEMM each).  tok/s = 2048 / step time.
 
+--workload ffn_swiglu runs one 7B feed-forward block the fused way: the gate
+and up projections as one pair GEMM whose epilogue writes the down projection's
+q8 input h = SiLU(gate) * up, then the down GEMM (compare --workload ffn, the
+three GEMMs with separate fp32 inputs).
+
 --workload decode runs the same 224 projections for one token (the small-M
 path, bound by reading 3.64 GB of packed weights), captured in a CUDA graph
 so that the timed region holds no host launch overhead.
@@ -41,6 +46,9 @@ WORKLOADS = {
             "7B FFN linears gate/up 11008x4096 + down 4096x11008 Q4_K, 2048 tokens, fused q8, bf16 out"),
     "qproj2630": (2630, [(4096, 4096)], "bf16", "7B q-proj 4096x4096 Q4_K, 2630 tokens (outlier channels), fused q8, bf16 out"),
     "qproj512": (512, [(4096, 4096)], "f32", "7B q-proj 4096x4096 Q4_K, 512 tokens, fused q8, fp32 out"),
+    "ffn_swiglu": (2048, [(22016, 4096), (4096, 11008)], "bf16",
+                   "7B FFN with the SiLU(gate)*up epilogue: gate+up 11008x4096 as one pair GEMM whose epilogue "
+                   "writes the q8 input of down 4096x11008, Q4_K, 2048 tokens, fused q8 of x, bf16 out"),
     "decode": (1, [(n, k) for _ in range(32) for (_, n, k) in LAYER], "bf16",
                "7B linear stack at decode size: 32 layers x {q,k,v,o 4096x4096; gate,up 11008x4096; down "
                "4096x11008} Q4_K, 1 token, fused q8 activation quantization, bf16 out (small-M path, "
@@ -173,6 +181,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     tokens, mats, out, desc = WORKLOADS[args.workload]
+    if args.workload == "ffn_swiglu":
+        return run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local)
     kind = "outlier" if args.workload == "qproj2630" else "normal"
     # weights (packed once, resident) and one activation matrix per projection
     packed, xs, ys = [], [], []
@@ -255,6 +265,110 @@ def main():
             "roofline": roofline, "clocks": clk, "gpu_launches": 2 * len(mats) * args.steps}
     if e2e is not None:
         line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"], _ = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
+    """The 7B FFN through the SiLU(gate)*up epilogue.  One step: quantize x
+    (2048 x 4096 fp32), the gate/up pair GEMM (22016 x 4096) whose epilogue
+    writes the q8 operand of h = SiLU(g) * u, and the down GEMM (4096 x 11008)
+    from it.  roofline: both GEMMs' 2*M*N*K flops / their CUDA-event time."""
+    tokens, mats, out, desc = WORKLOADS[args.workload]
+    nf, k = 11008, 4096
+    gate = inputs.q4k_blocks_torch(nf, k, seed=4 + rank, tag=0, device=dev)
+    up = inputs.q4k_blocks_torch(nf, k, seed=4 + rank, tag=1, device=dev)
+    pair = q4k.q4k_pack_swiglu_weights(gate, up, nf, k)
+    del gate, up
+    down_blocks = inputs.q4k_blocks_torch(4096, nf, seed=4 + rank, tag=2, device=dev)
+    down = q4k.q4k_pack_weights(down_blocks, 4096, nf)
+    del down_blocks
+    x = inputs.activations_torch(tokens, k, seed=4 + rank, kind="normal", tag=0, device=dev)
+    ws = torch.empty(q4k.q4k_act_workspace_bytes(tokens, k), dtype=torch.uint8, device=dev)
+    h_ws = torch.empty(q4k.q4k_act_workspace_bytes(tokens, nf), dtype=torch.uint8, device=dev)
+    y = torch.empty((tokens, 4096), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        q4k.q4k_act_quantize(x, workspace=ws, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        q4k.q4k_gemm_swiglu_quantized(pair, nf, k, ws, tokens, h_ws=h_ws, stream=stream)
+        q4k.q4k_gemm_quantized(down, 4096, nf, h_ws, tokens, out, y=y, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s_ in range(args.steps):
+        step(evs[s_])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    err = q4k.q4k_device_error_word()
+    if err:
+        raise RuntimeError(f"device error word 0x{err:x}")
+    ms_step = total_ms / args.steps
+    gemm_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    flops_step = sum(2.0 * tokens * n * kk for n, kk in mats)
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops_step / (gemm_ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": world * tokens / (ms_step * 1e-3), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers",
+            "data": "synthetic (seeded random Q4_K weights and activations)",
+            "config": {"workload": desc, "tokens": tokens, "gemms_per_step": 2,
+                       "l2": "weights 76 MB + 25 MB, activations 34 MB in / 45 MB between the GEMMs",
+                       "parallelism": f"replicas x{world}"},
+            "effective_tops": world * flops_step / (ms_step * 1e-3) / 1e12, "gemm_ms_per_step": gemm_ms,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "q4k_gemm_kernel",
+                         "peak_source": f"{src} bf16 dense, sustained",
+                         "per_launch": "2*M*N*K of the pair and down GEMMs / their CUDA-event time per step"},
+            "clocks": clk, "gpu_launches": 3 * args.steps}
+    if not args.no_e2e and rank == 0:
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hx.copy_(x)
+        hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        dx = torch.empty_like(x)
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            q4k.q4k_gemm_swiglu(pair, nf, k, dx, h_ws=h_ws, workspace=ws, stream=stream)
+            q4k.q4k_gemm_quantized(down, 4096, nf, h_ws, tokens, out, y=y, stream=stream)
+            hy.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / 3
+        line["e2e"] = {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": tokens * k * 4,
+                       "d2h_bytes_per_step": tokens * 4096 * 2, "ms_per_step": ms, "steps": 3}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"], _ = cpu_baseline(args.workload)
     if rank == 0:

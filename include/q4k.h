@@ -155,6 +155,53 @@ q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k,
                               void* y, int out_dtype, int64_t ldy, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Gate/up pair with a SiLU(gate)*up epilogue that produces the down
+ * projection's quantized input.  The pages measure LLaMA-7B's linear layers
+ * ("34 · r31 — q-major sda scale-read repack", Result: 7B q4_K whole-prefill);
+ * its feed-forward block feeds the down projection h = SiLU(g) * u with
+ * g = W_gate x, u = W_up x and SiLU(g) = g / (1 + e^-g).  Fusing it into the
+ * gate/up product's epilogue removes the round trip of g and u through HBM
+ * and the separate activation quantization of h.
+ *
+ * q4k_pack_swiglu_weights  gate and up Q4_K blocks ([n][k/256] x 144 B each,
+ *            device, 16-byte aligned) -> one packed matrix of 2n rows in
+ *            which each 128-row tile holds 64 outputs' gate and up rows;
+ *            packed: q4k_swiglu_packed_bytes(n, k) bytes, 256-byte aligned.
+ * q4k_gemm_swiglu  x (act and x_or_q8, da_f16, ssum, m, ldx as for q4k_gemm)
+ *            times the pair; h_ws receives, for every token, the q8
+ *            quantization of h (32-element blocks along n, the same rule as
+ *            q8_quantize_rows) in the operand form of q4k_act_quantize for
+ *            an m x n input: pass it to q4k_gemm_quantized with the down
+ *            projection's weights (k = n).
+ *            h_ws: >= q4k_act_workspace_bytes(m, n) bytes, 256-byte aligned;
+ *            workspace: >= q4k_gemm_workspace_bytes(m, 2n, k, act), scratch
+ *            for x's operand form; the two must not overlap.
+ * h is evaluated in a fixed fp32 order, each step one IEEE round-to-nearest
+ * operation.  With t = -g: SiLU = -0 if t > 80; SiLU = g if t < -87;
+ * otherwise SiLU = RN(g * R(RN(1 + E(t)))); then h = RN(SiLU * u).
+ * E(t) = RN(p(r) * 2^n) where n = rint_even(RN(t * RN32(log2 e))),
+ * r = RN(RN(t - n*355/512) - RN(n*C2)), C2 = RN32(ln 2 - 355/512), and p is
+ * the degree-7 Taylor polynomial of e^r in Horner form with fp32 coefficients
+ * RN32(1/j!) (each step RN(RN(p*r) + c)).  R(s): y = the float with bits
+ * 0x7EF311C2 - bits(s), then three times y = RN(y * RN(2 - RN(s * y))).
+ * g and u are the fp32 values the same product writes with f32 output.
+ * Packing needs n % 64 == 0; q4k_gemm_swiglu needs n % 256 == 0 (n is the
+ * down projection's k), k % 256 == 0, m >= 0.
+ * ------------------------------------------------------------------------ */
+size_t q4k_swiglu_packed_bytes(int64_t n, int64_t k);
+q4k_status q4k_pack_swiglu_weights(const void* gate_blocks, const void* up_blocks, int64_t n, int64_t k,
+                                   void* packed, size_t packed_bytes, cudaStream_t stream);
+q4k_status q4k_gemm_swiglu(const void* packed_pair, int64_t n, int64_t k,
+                           int act, const void* x_or_q8, const void* da_f16, const void* ssum,
+                           int64_t m, int64_t ldx, void* h_ws, size_t h_ws_bytes,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+/* The second half of q4k_gemm_swiglu, for x already in operand form (from
+ * q4k_act_quantize or q4k_act_from_q8 with the same m and k). */
+q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t k,
+                                     const void* workspace, size_t workspace_bytes, int64_t m,
+                                     void* h_ws, size_t h_ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * q4k_gemm_static_workspace -- q4k_gemm without a workspace argument.
  * Library addition with no counterpart in the pages: it exists for callers
  * that cannot hand the library scratch memory, e.g. a plain C host that holds

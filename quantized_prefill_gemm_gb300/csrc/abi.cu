@@ -134,11 +134,14 @@ q4k_status check_output(const void* y, int64_t m, int64_t n, int out, int64_t ld
     return Q4K_OK;
 }
 
+// h_ws (gate/up pair weights only): instead of Y, write the down projection's
+// operand of SiLU(gate)*up, ActLayout(m, n / 2), there; y, out and ldy are then
+// unused.  The caller has checked h_ws.
 q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, size_t ws_bytes, int64_t m, void* y,
-                    int out, int64_t ldy, float* dbg, cudaStream_t stream) {
+                    int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream) {
     q4k_status st = check_gemm_shape(n, k, m);
     if (st != Q4K_OK) return st;
-    if ((st = check_output(y, m, n, out, ldy)) != Q4K_OK) return st;
+    if (!h_ws && (st = check_output(y, m, n, out, ldy)) != Q4K_OK) return st;
     if (!packed_w || (m > 0 && !ws)) return Q4K_ERR_INVALID_ARG;
     if (!aligned(packed_w, 256) || (m > 0 && !aligned(ws, 256))) return Q4K_ERR_ALIGNMENT;
     const ActLayout A(m, k);
@@ -178,6 +181,14 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
     p.n_zst = static_cast<int>(3 * ((kc + 63) / 64));
     p.n_main = static_cast<int>(k / 64);
     p.out_bf16 = out == Q4K_OUT_BF16 ? 1 : 0;
+    if (h_ws) {
+        const ActLayout H(m, n / 2);
+        uint8_t* hb = static_cast<uint8_t*>(h_ws);
+        p.hq = reinterpret_cast<__half*>(hb + H.xq);
+        p.hda = reinterpret_cast<float*>(hb + H.da);
+        p.he = reinterpret_cast<__nv_bfloat16*>(hb + H.e);
+        p.hkc = static_cast<int>(n / 64);
+    }
     const int grid = std::min(p.num_tiles, dev->sm_count);
     return from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream));
 }
@@ -287,6 +298,24 @@ q4k_status q4k_pack_weights(const void* blocks, int64_t n, int64_t k, void* pack
     return from_cuda(launch_pack(static_cast<const uint8_t*>(blocks), n, k, static_cast<uint8_t*>(packed), stream));
 }
 
+size_t q4k_swiglu_packed_bytes(int64_t n, int64_t k) {
+    if (n <= 0 || n % 64 || n >= kMaxDim / 2) return 0;
+    return q4k_packed_bytes(2 * n, k);
+}
+
+q4k_status q4k_pack_swiglu_weights(const void* gate_blocks, const void* up_blocks, int64_t n, int64_t k,
+                                   void* packed, size_t packed_bytes, cudaStream_t stream) {
+    if (n <= 0 || k <= 0 || n % 64 || k % 256 || n >= kMaxDim / 2 || k >= kMaxDim) return Q4K_ERR_SHAPE;
+    if (!gate_blocks || !up_blocks || !packed) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(gate_blocks, 16) || !aligned(up_blocks, 16) || !aligned(packed, 256)) return Q4K_ERR_ALIGNMENT;
+    if (packed_bytes < q4k_swiglu_packed_bytes(n, k)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    return from_cuda(launch_pack_pair(static_cast<const uint8_t*>(gate_blocks), static_cast<const uint8_t*>(up_blocks),
+                                      n, k, static_cast<uint8_t*>(packed), stream));
+}
+
 size_t q4k_act_workspace_bytes(int64_t m, int64_t k) {
     if (m < 0 || k <= 0 || k % 256 || m >= kMaxDim || k >= kMaxDim) return 0;
     return static_cast<size_t>(ActLayout(m, k).total);
@@ -329,7 +358,7 @@ q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16
 q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k, const void* workspace,
                               size_t workspace_bytes, int64_t m, void* y, int out_dtype, int64_t ldy,
                               cudaStream_t stream) {
-    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, stream);
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream);
 }
 
 q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const void* x_or_q8, const void* da_f16,
@@ -374,7 +403,45 @@ q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
                              static_cast<const int16_t*>(ssum), m, k, ldx, workspace, workspace_bytes, stream);
     }
     if (st != Q4K_OK) return st;
-    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, stream);
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream);
+}
+
+q4k_status q4k_gemm_swiglu(const void* packed_pair, int64_t n, int64_t k, int act, const void* x_or_q8,
+                           const void* da_f16, const void* ssum, int64_t m, int64_t ldx, void* h_ws,
+                           size_t h_ws_bytes, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (n <= 0 || n % 256 || n >= kMaxDim / 2) return Q4K_ERR_SHAPE;   // n is the down projection's k
+    q4k_status st = check_gemm_shape(2 * n, k, m);
+    if (st != Q4K_OK) return st;
+    if (!packed_pair) return Q4K_ERR_INVALID_ARG;
+    if (act != Q4K_ACT_F32 && act != Q4K_ACT_Q8) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(packed_pair, 256)) return Q4K_ERR_ALIGNMENT;
+    if (m == 0) return Q4K_OK;
+    if (!h_ws) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(h_ws, 256)) return Q4K_ERR_ALIGNMENT;
+    if (h_ws_bytes < static_cast<size_t>(ActLayout(m, n).total)) return Q4K_ERR_WORKSPACE;
+    if (act == Q4K_ACT_F32) {
+        st = q4k_act_quantize(static_cast<const float*>(x_or_q8), m, k, ldx, workspace, workspace_bytes, stream);
+    } else {
+        st = q4k_act_from_q8(static_cast<const int8_t*>(x_or_q8), static_cast<const uint16_t*>(da_f16),
+                             static_cast<const int16_t*>(ssum), m, k, ldx, workspace, workspace_bytes, stream);
+    }
+    if (st != Q4K_OK) return st;
+    return run_gemm(packed_pair, 2 * n, k, workspace, workspace_bytes, m, nullptr, Q4K_OUT_F32, 2 * n, nullptr, h_ws,
+                    stream);
+}
+
+q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t k, const void* workspace,
+                                     size_t workspace_bytes, int64_t m, void* h_ws, size_t h_ws_bytes,
+                                     cudaStream_t stream) {
+    if (n <= 0 || n % 256 || n >= kMaxDim / 2) return Q4K_ERR_SHAPE;
+    q4k_status st = check_gemm_shape(2 * n, k, m);
+    if (st != Q4K_OK) return st;
+    if (m == 0) return Q4K_OK;
+    if (!h_ws) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(h_ws, 256)) return Q4K_ERR_ALIGNMENT;
+    if (h_ws_bytes < static_cast<size_t>(ActLayout(m, n).total)) return Q4K_ERR_WORKSPACE;
+    return run_gemm(packed_pair, 2 * n, k, workspace, workspace_bytes, m, nullptr, Q4K_OUT_F32, 2 * n, nullptr, h_ws,
+                    stream);
 }
 
 unsigned int q4k_device_error_word(int reset) {
@@ -415,7 +482,7 @@ q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, 
                                     cudaStream_t stream) {
     if (!chunk_acc) return Q4K_ERR_INVALID_ARG;
     if (m < 0 || n <= 0 || k <= 0 || m * n * (k / 32) > (int64_t(1) << 26)) return Q4K_ERR_SHAPE;
-    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, Q4K_OUT_F32, ldy, chunk_acc, stream);
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, Q4K_OUT_F32, ldy, chunk_acc, nullptr, stream);
 }
 
 }  // extern "C"

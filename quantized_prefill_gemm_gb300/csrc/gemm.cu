@@ -300,6 +300,95 @@ __device__ __forceinline__ void store_row16(const GemmParams& p, int64_t t, int 
     }
 }
 
+// ---------------------------------------------- SiLU(gate)*up epilogue --
+// h = SiLU(g) * u for the down projection, in a fixed fp32 operation order so
+// that the q8 codes it yields are reproducible bit for bit: every step is one
+// IEEE operation (the _rn intrinsics are never contracted into FMAs).  With
+// t = -g:
+//   t > 80:   SiLU = RN(g * 0) = -0
+//   t < -87:  SiLU = g
+//   else:     SiLU = RN(g * R(RN(1 + E(t))))
+//   h = RN(SiLU * u)
+// E(t) ~ e^t: Cody and Waite's reduction t = n ln2 + r with ln2 split into
+// C1 = 355/512 (n*C1 exact) and C2 = RN(ln2 - C1), the degree-7 Taylor
+// polynomial of e^r in Horner form, and an exact scaling by 2^n (within
+// 1.2 ulp).  R(s) ~ 1/s: a seed read off the bits of s (0x7EF311C2 minus
+// them), then three Newton steps y = RN(y * RN(2 - RN(s * y))) (within 2 ulp
+// for s in [1, 6e34]).  Everything is branch-free, so that the compiler can
+// interleave the 32 elements of a thread.  Constants: the fp32 roundings of
+// log2(e), C1, C2 and 1/j!.
+__device__ __forceinline__ float silu_mul_fixed(float g, float u) {
+    const float t = -g;
+    const float tc = fminf(fmaxf(t, -87.0f), 80.0f);
+    const float n = rintf(__fmul_rn(tc, 0x1.715476p+0f));
+    const float r = __fsub_rn(__fsub_rn(tc, __fmul_rn(n, 0x1.63p-1f)), __fmul_rn(n, -0x1.bd0106p-13f));
+    float p = 0x1.a01a02p-13f;                         // 1/7!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);   // 1/6!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);    // 1/5!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);    // 1/4!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);    // 1/3!
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    const float e = __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
+    const float s = __fadd_rn(1.0f, e);
+    float y = __int_as_float(0x7EF311C2 - __float_as_int(s));
+#pragma unroll
+    for (int i = 0; i < 3; ++i) y = __fmul_rn(y, __fsub_rn(2.0f, __fmul_rn(s, y)));
+    float silu = __fmul_rn(g, y);
+    silu = t > 80.0f ? __fmul_rn(g, 0.0f) : silu;
+    silu = t < -87.0f ? g : silu;
+    return __fmul_rn(silu, u);
+}
+
+// Tile end of the gate/up pair GEMM: this thread holds, for token t, the 32
+// gate outputs (TMEM columns 0-31 of its 64) and the 32 up outputs of the same
+// features (columns 32-63).  It forms h, quantizes it as one 32-element q8
+// block (chunk c of the down projection's input; the same rule as
+// q8_quantize_rows: d = RN(amax/127), inv = RN(127/amax),
+// qa = clamp(rint_even(RN(h*inv)), -127, 127), d_a = RN16(d), a block with
+// amax < 2^-120 is zero) and writes the down projection's operand: fp16 qa,
+// fp32 d_a and the hi/lo bf16 split of d_a*ssum.
+__device__ __forceinline__ void swiglu_store(const GemmParams& p, int64_t t, int c, const uint32_t (&g0)[16],
+                                             const uint32_t (&g1)[16], const uint32_t (&u0)[16],
+                                             const uint32_t (&u1)[16]) {
+    float h[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        h[i] = silu_mul_fixed(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
+        h[16 + i] = silu_mul_fixed(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
+    }
+    float amax = fabsf(h[0]);
+#pragma unroll
+    for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    const bool live = amax >= 0x1p-120f;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __fdiv_rn(127.0f, amax);
+    int ssum = 0;
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        int q0 = max(-127, min(127, __float2int_rn(__fmul_rn(h[i], inv))));
+        int q1 = max(-127, min(127, __float2int_rn(__fmul_rn(h[i + 1], inv))));
+        q0 = live ? q0 : 0;
+        q1 = live ? q1 : 0;
+        ssum += q0 + q1;
+        const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+        w[i >> 1] = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    const int64_t kd = static_cast<int64_t>(p.hkc) * 32;
+    uint4* dst = reinterpret_cast<uint4*>(p.hq + t * kd + 32 * c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    const __half da = __float2half_rn(live ? d : 0.0f);
+    p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = __half2float(da);
+    const float e = __fmul_rn(__half2float(da), static_cast<float>(ssum));   // exact: 11 x <= 13 bits
+    const __nv_bfloat16 hi = __float2bfloat16_rn(e);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(e, __bfloat162float(hi)));
+    p.he[t * p.hkc + c] = hi;
+    p.he[(static_cast<int64_t>(p.m) + t) * p.hkc + c] = lo;
+}
+
 __device__ __forceinline__ void dump_chunk(const GemmParams& p, int64_t t, int col, int64_t c, const uint32_t (&J)[16]) {
     if (t >= p.m) return;
 #pragma unroll 4
@@ -309,7 +398,7 @@ __device__ __forceinline__ void dump_chunk(const GemmParams& p, int64_t t, int c
 // Warp e (0..7) reads TMEM lanes 32*(warp%4)..+31 (the lane quadrant its
 // warp index allows) and columns 64*(e/4)..+63 of each buffer: each thread
 // owns one token row and 64 output columns.
-template <bool kDump>
+template <bool kDump, bool kSwiGLU>
 __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p, int warp, int e, int lane) {
     const int n_st = p.n_zst + p.n_main;
     const int qd = warp & 3, ch = e >> 2;
@@ -402,22 +491,43 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
             advance(s, ph);
         }
         if (!ok) break;
-        // tile done: Y (TMEM) -> HBM
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t Yv[16];
-            tmem_ld16(ty + 16u * q, Yv);
+        if constexpr (kSwiGLU) {
+            // tile done: the 64 columns are 32 gate and 32 up outputs of the
+            // down projection's input chunk c = 2 nt + ch
+            uint32_t g0[16], g1[16], u0[16], u1[16];
+            tmem_ld16(ty, g0);
+            tmem_ld16(ty + 16u, g1);
+            tmem_ld16(ty + 32u, u0);
+            tmem_ld16(ty + 48u, u1);
             tmem_wait_ld();
-            if (t < p.m) store_row16(p, t, col0 + 16 * q, Yv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
+            const int c = 2 * nt + ch;
+            if (t < p.m)
+                swiglu_store(p, t, c, g0, g1, u0, u1);
+            else   // padding token of the last 128-token tile: scale 0
+                p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = 0.0f;
+        } else {
+            // tile done: Y (TMEM) -> HBM
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t Yv[16];
+                tmem_ld16(ty + 16u * q, Yv);
+                tmem_wait_ld();
+                if (t < p.m) store_row16(p, t, col0 + 16 * q, Yv);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
     }
 }
 
 // kDump: also write every per-chunk accumulator to p.dbg (test hook build).
-template <bool kDump>
+// kSwiGLU: gate/up pair weights; the tile end writes the down projection's
+// q8 operand of SiLU(gate)*up instead of Y.
+template <bool kDump, bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     q4k_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_e,
                     const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
@@ -466,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 6) {
         run_converter(cx, p, warp - 2, lane);
     } else {
-        run_epilogue<kDump>(cx, p, warp, warp - 6, lane);
+        run_epilogue<kDump, kSwiGLU>(cx, p, warp, warp - 6, lane);
     }
 
     tc_fence_before();
@@ -495,24 +605,22 @@ __global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_cycles) {
 
 cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                         const GemmParams& p, int grid, cudaStream_t s) {
-    static bool attr_set[64][2] = {};
+    static bool attr_set[64][3] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int dump = p.dbg != nullptr ? 1 : 0;
-    if (!attr_set[dev][dump]) {
-        e = dump ? cudaFuncSetAttribute(q4k_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kSmemBytes))
-                 : cudaFuncSetAttribute(q4k_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kSmemBytes));
+    if (p.dbg && p.hq) return cudaErrorInvalidValue;
+    const int variant = p.dbg ? 1 : (p.hq ? 2 : 0);
+    void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const GemmParams) =
+        variant == 1 ? q4k_gemm_kernel<true, false> : (variant == 2 ? q4k_gemm_kernel<false, true>
+                                                                     : q4k_gemm_kernel<false, false>);
+    if (!attr_set[dev][variant]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
-        attr_set[dev][dump] = true;
+        attr_set[dev][variant] = true;
     }
-    if (dump)
-        q4k_gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
-    else
-        q4k_gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
+    kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
     return cudaGetLastError();
 }
 

@@ -14,6 +14,12 @@
 // GEMM, and for the small-M path the m bytes and the fp32 dmin of each
 // super-block.  One thread per (od row, super-block); runs once per weight
 // matrix.
+//
+// Gate/up pairs (for the SiLU(gate)*up epilogue): the packed matrix has 2n
+// rows; packed row R of tile T = R / 128 takes, for j = (R % 128) / 32 and
+// i = R % 32, row 64 T + 32 (j / 2) + i of the gate (j even) or up (j odd)
+// matrix.  So each half of a 128-row tile holds 32 gate rows and the 32 up
+// rows of the same outputs, side by side.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -25,7 +31,10 @@ namespace {
 
 constexpr int kThreadsPerBlock = 128;
 
-__global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* __restrict__ blocks, int64_t n,
+// blocks: [n][k/256] canonical blocks; up: null, or the up matrix of a gate
+// (blocks) / up pair, n then being the packed row count 2 x (rows of each).
+__global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* __restrict__ blocks,
+                                                                const uint8_t* __restrict__ up, int64_t n,
                                                                 int64_t k, uint8_t* __restrict__ packed,
                                                                 int64_t off_sc, int64_t off_dsb, int64_t off_ndm,
                                                                 int64_t off_mq, int64_t off_dmn) {
@@ -34,6 +43,11 @@ __global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* _
     if (idx >= n * ksb) return;
     const int64_t o = idx / ksb, sb = idx % ksb;
     const uint8_t* blk = blocks + idx * 144;
+    if (up) {
+        const int64_t j = (o & 127) >> 5;
+        const int64_t src = 64 * (o >> 7) + 32 * (j >> 1) + (o & 31);
+        blk = ((j & 1) ? up : blocks) + (src * ksb + sb) * 144;
+    }
 
     const uint32_t head = *reinterpret_cast<const uint32_t*>(blk);
     const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(head & 0xFFFFu)));
@@ -101,7 +115,17 @@ cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* pa
     const int64_t threads = n * (k / 256);
     if (threads == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((threads + kThreadsPerBlock - 1) / kThreadsPerBlock);
-    pack_kernel<<<grid, kThreadsPerBlock, 0, s>>>(blocks, n, k, packed, L.sc, L.dsb, L.ndm, L.mq, L.dmn);
+    pack_kernel<<<grid, kThreadsPerBlock, 0, s>>>(blocks, nullptr, n, k, packed, L.sc, L.dsb, L.ndm, L.mq, L.dmn);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_pair(const uint8_t* gate, const uint8_t* up, int64_t n, int64_t k, uint8_t* packed,
+                             cudaStream_t s) {
+    const PackedLayout L(2 * n, k);
+    const int64_t threads = 2 * n * (k / 256);
+    if (threads == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((threads + kThreadsPerBlock - 1) / kThreadsPerBlock);
+    pack_kernel<<<grid, kThreadsPerBlock, 0, s>>>(gate, up, 2 * n, k, packed, L.sc, L.dsb, L.ndm, L.mq, L.dmn);
     return cudaGetLastError();
 }
 

@@ -2,6 +2,8 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace q4k {
@@ -21,6 +23,13 @@ struct GemmParams {
     int m_tiles, n_tiles, num_tiles;
     int n_zst, n_main;      // min-term stages and main stages per tile
     int out_bf16;
+    // SiLU(gate)*up epilogue (gate/up pair weights, y unused): the down
+    // projection's activation operand for kd = n / 2 inputs, in the
+    // q4k_act_quantize layout (q4k_layout.h, ActLayout(m, kd))
+    __half* hq;             // [m][kd] fp16 qa
+    float* hda;             // [mp/128][kd/32][128] d_a
+    __nv_bfloat16* he;      // [2][m][kd/32] d_a*ssum hi / lo
+    int hkc;                // kd / 32
 };
 
 // Small-M product (gemv.cu): packed weights as for the GEMM, activations as
@@ -48,6 +57,9 @@ cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ld
 cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
                                int64_t ldq, void* ws, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
+// gate and up [n][k/256] blocks each -> one packed matrix of 2n interleaved rows
+cudaError_t launch_pack_pair(const uint8_t* gate, const uint8_t* up, int64_t n, int64_t k, uint8_t* packed,
+                             cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                         const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);

@@ -45,6 +45,12 @@ SIGNATURES = {
     "q4k_selftest_wait_timeout": (_c_int, [_c_i64, _c_ptr]),
     "q4k_gemm_debug_chunk_acc": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_i64,
                                           _c_ptr, _c_ptr]),
+    "q4k_swiglu_packed_bytes": (_c_size, [_c_i64, _c_i64]),
+    "q4k_pack_swiglu_weights": (_c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_ptr]),
+    "q4k_gemm_swiglu": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
+                                 _c_ptr, _c_size, _c_ptr, _c_size, _c_ptr]),
+    "q4k_gemm_swiglu_quantized": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_size,
+                                           _c_ptr]),
     "q4k_static_workspace_bytes": (_c_size, []),
     "q4k_gemm_static_workspace": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
                                            _c_ptr, _c_int, _c_i64, _c_ptr]),
@@ -201,6 +207,53 @@ def q4k_gemm(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, out_dtype="f
         _dev(ssum, "ssum", torch.int16) if act == ACT_Q8 else None,
         m, ldx, _dev(y, "y"), code, ldy, _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
     return y
+
+
+def q4k_swiglu_packed_bytes(n: int, k: int) -> int:
+    return int(LIB.q4k_swiglu_packed_bytes(n, k))
+
+
+def q4k_pack_swiglu_weights(gate_blocks: torch.Tensor, up_blocks: torch.Tensor, n: int, k: int, packed=None,
+                            stream=None) -> torch.Tensor:
+    """gate and up Q4_K blocks (uint8 [n][k/256*144] each, on the device) -> packed pair."""
+    nb = q4k_swiglu_packed_bytes(n, k)
+    if nb == 0:
+        raise ValueError(f"unsupported gate/up shape n={n} k={k}")
+    packed = _workspace(nb, gate_blocks.device, packed)
+    _check("q4k_pack_swiglu_weights", LIB.q4k_pack_swiglu_weights(
+        _dev(gate_blocks, "gate_blocks", torch.uint8), _dev(up_blocks, "up_blocks", torch.uint8), n, k,
+        _dev(packed, "packed"), packed.numel(), _stream(stream)))
+    return packed
+
+
+def q4k_gemm_swiglu(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, da=None, ssum=None, h_ws=None,
+                    workspace=None, stream=None) -> torch.Tensor:
+    """SiLU(x W_gate^T) * (x W_up^T), quantized for the down projection: returns the
+    operand workspace (uint8) to pass to q4k_gemm_quantized(down, n_down, n, h_ws, m)."""
+    m, kx, ldx = _row_major(x, "x")
+    if kx != k:
+        raise ValueError("x has the wrong number of columns")
+    act = ACT_Q8 if x.dtype == torch.int8 else ACT_F32
+    if act == ACT_Q8 and (da is None or ssum is None):
+        raise ValueError("q8 input needs da and ssum")
+    h_ws = _workspace(q4k_act_workspace_bytes(m, n), x.device, h_ws)
+    workspace = _workspace(q4k_gemm_workspace_bytes(m, 2 * n, k, act), x.device, workspace)
+    _check("q4k_gemm_swiglu", LIB.q4k_gemm_swiglu(
+        _dev(packed, "packed"), n, k, act, _dev(x, "x"),
+        _dev(da, "da", torch.float16) if act == ACT_Q8 else None,
+        _dev(ssum, "ssum", torch.int16) if act == ACT_Q8 else None,
+        m, ldx, _dev(h_ws, "h_ws"), h_ws.numel(), _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return h_ws
+
+
+def q4k_gemm_swiglu_quantized(packed: torch.Tensor, n: int, k: int, workspace: torch.Tensor, m: int, h_ws=None,
+                              stream=None) -> torch.Tensor:
+    """q4k_gemm_swiglu for x already in operand form (q4k_act_quantize / q4k_act_from_q8)."""
+    h_ws = _workspace(q4k_act_workspace_bytes(m, n), workspace.device, h_ws)
+    _check("q4k_gemm_swiglu_quantized", LIB.q4k_gemm_swiglu_quantized(
+        _dev(packed, "packed"), n, k, _dev(workspace, "workspace"), workspace.numel(), m, _dev(h_ws, "h_ws"),
+        h_ws.numel(), _stream(stream)))
+    return h_ws
 
 
 def q4k_static_workspace_bytes() -> int:
