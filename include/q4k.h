@@ -142,7 +142,12 @@ q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k,
  * q4k_act_quantize   fp32 x [m][ldx] -> the GEMM operand form in `workspace`
  * q4k_act_from_q8    q8 SoA (as q8_quantize_rows writes it) -> same form
  * q4k_gemm_quantized workspace (filled by one of the two, same m and k) -> Y
- * workspace: >= q4k_act_workspace_bytes(m, k) bytes, 256-byte aligned.
+ * workspace: >= q4k_act_workspace_bytes(m, k) bytes, 256-byte aligned.  The
+ * operand part is only read by the GEMM and may feed any number of calls;
+ * the GEMM also uses a scratch part of the workspace (about 10 MB, for the
+ * partial tiles of the work it splits along k to balance the last wave over
+ * the SMs), so GEMMs that may run at the same time (different streams) must
+ * not share a workspace.
  * ------------------------------------------------------------------------ */
 size_t q4k_act_workspace_bytes(int64_t m, int64_t k);
 q4k_status q4k_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx,
@@ -151,7 +156,7 @@ q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16
                            int64_t m, int64_t k, int64_t ldq,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k,
-                              const void* workspace, size_t workspace_bytes, int64_t m,
+                              void* workspace, size_t workspace_bytes, int64_t m,
                               void* y, int out_dtype, int64_t ldy, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -198,7 +203,7 @@ q4k_status q4k_gemm_swiglu(const void* packed_pair, int64_t n, int64_t k,
 /* The second half of q4k_gemm_swiglu, for x already in operand form (from
  * q4k_act_quantize or q4k_act_from_q8 with the same m and k). */
 q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t k,
-                                     const void* workspace, size_t workspace_bytes, int64_t m,
+                                     void* workspace, size_t workspace_bytes, int64_t m,
                                      void* h_ws, size_t h_ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -253,7 +258,7 @@ unsigned int q4k_device_error_word(int reset);
 q4k_status q4k_device_status(int reset);
 q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
 q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k,
-                                    const void* workspace, size_t workspace_bytes, int64_t m,
+                                    void* workspace, size_t workspace_bytes, int64_t m,
                                     float* y, int64_t ldy, float* chunk_acc, cudaStream_t stream);
 
 #ifdef __cplusplus

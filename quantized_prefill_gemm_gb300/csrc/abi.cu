@@ -137,7 +137,7 @@ q4k_status check_output(const void* y, int64_t m, int64_t n, int out, int64_t ld
 // h_ws (gate/up pair weights only): instead of Y, write the down projection's
 // operand of SiLU(gate)*up, ActLayout(m, n / 2), there; y, out and ldy are then
 // unused.  The caller has checked h_ws.
-q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, size_t ws_bytes, int64_t m, void* y,
+q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t ws_bytes, int64_t m, void* y,
                     int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream) {
     q4k_status st = check_gemm_shape(n, k, m);
     if (st != Q4K_OK) return st;
@@ -152,7 +152,7 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
 
     const PackedLayout W(n, k);
     const uint8_t* wb = static_cast<const uint8_t*>(packed_w);
-    const uint8_t* ab = static_cast<const uint8_t*>(ws);
+    uint8_t* ab = static_cast<uint8_t*>(ws);
     const int64_t kc = k / 32;
     CUtensorMap tm_x, tm_e, tm_d;
     if ((st = encode_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ab + A.xq, k, m, 1)) != Q4K_OK) return st;
@@ -181,6 +181,28 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
     p.n_zst = static_cast<int>(3 * ((kc + 63) / 64));
     p.n_main = static_cast<int>(k / 64);
     p.out_bf16 = out == Q4K_OUT_BF16 ? 1 : 0;
+    // Tail balance: after the last full wave of tiles over the SMs, the R
+    // remaining tiles are split along k into parts (whole super-blocks) so
+    // that R x parts work units occupy the otherwise idle SMs.  The epilogue
+    // writes each part's partial tile to the workspace; a small kernel then
+    // adds a tile's parts in part order (deterministic) and finishes the tile
+    // as usual, so Y, or the SiLU(gate)*up operand, comes from the same fp32
+    // sums whichever output the call asks for.
+    p.split = 1;
+    p.part_sb = p.ksb;
+    p.full_tiles = p.num_tiles;
+    const int sms = std::min<int>(dev->sm_count, static_cast<int>(kMaxSplitUnits));
+    const int rem = p.num_tiles % sms;
+    if (rem > 0) {
+        const int parts = std::min(sms / rem, p.ksb);
+        if (parts >= 2) {
+            p.part_sb = (p.ksb + parts - 1) / parts;
+            p.split = (p.ksb + p.part_sb - 1) / p.part_sb;
+            p.full_tiles = p.num_tiles - rem;
+        }
+    }
+    p.num_units = p.full_tiles + (p.num_tiles - p.full_tiles) * p.split;
+    p.part = reinterpret_cast<float*>(ab + A.part);
     if (h_ws) {
         const ActLayout H(m, n / 2);
         uint8_t* hb = static_cast<uint8_t*>(h_ws);
@@ -189,8 +211,9 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, const void* ws, 
         p.he = reinterpret_cast<__nv_bfloat16*>(hb + H.e);
         p.hkc = static_cast<int>(n / 64);
     }
-    const int grid = std::min(p.num_tiles, dev->sm_count);
-    return from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream));
+    const int grid = std::min(p.num_units, dev->sm_count);
+    if ((st = from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream))) != Q4K_OK) return st;
+    return p.split > 1 ? from_cuda(launch_split_fixup(p, stream)) : Q4K_OK;
 }
 
 // Small-M path on the CUDA cores: the packed weights times either the q8 SoA
@@ -355,7 +378,7 @@ q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16
     return from_cuda(launch_act_from_q8(q8, da_f16, ssum, m, k, ldq, workspace, stream));
 }
 
-q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k, const void* workspace,
+q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k, void* workspace,
                               size_t workspace_bytes, int64_t m, void* y, int out_dtype, int64_t ldy,
                               cudaStream_t stream) {
     return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream);
@@ -430,7 +453,7 @@ q4k_status q4k_gemm_swiglu(const void* packed_pair, int64_t n, int64_t k, int ac
                     stream);
 }
 
-q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t k, const void* workspace,
+q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t k, void* workspace,
                                      size_t workspace_bytes, int64_t m, void* h_ws, size_t h_ws_bytes,
                                      cudaStream_t stream) {
     if (n <= 0 || n % 256 || n >= kMaxDim / 2) return Q4K_ERR_SHAPE;
@@ -477,7 +500,7 @@ q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
     return q4k_device_status(1);
 }
 
-q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, const void* workspace,
+q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, void* workspace,
                                     size_t workspace_bytes, int64_t m, float* y, int64_t ldy, float* chunk_acc,
                                     cudaStream_t stream) {
     if (!chunk_acc) return Q4K_ERR_INVALID_ARG;

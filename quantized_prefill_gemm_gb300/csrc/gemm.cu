@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include "q4k_internal.h"
+#include "q4k_layout.h"
 #include "q4k_ptx.cuh"
 
 namespace q4k {
@@ -108,28 +109,62 @@ __device__ __forceinline__ void advance(int& s, uint32_t& ph) {
     }
 }
 
+// One work unit: a whole tile, or one k-part of a tail tile (GemmParams).
+// Its stages st = 0 .. n_st-1 map to kb = st + kbase: kb < 0 are the
+// min-term stages (a unit has all of them or none: only whole tiles and part
+// 0 have them, and those start at kb = 0), kb >= 0 the 64-k main stages.
+struct Unit {
+    int mt, nt;
+    int kbase;      // first main stage minus the number of min-term stages
+    int n_st;       // stages of this unit
+    int slot;       // tail tile x split + part for a k-part, -1 for a whole tile
+};
+
+__device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
+    Unit w;
+    int tile;
+    if (u < p.full_tiles) {
+        tile = u;
+        w.slot = -1;
+        w.kbase = -p.n_zst;
+        w.n_st = p.n_zst + p.n_main;
+    } else {
+        const int v = u - p.full_tiles;
+        const int tail = v / p.split, part = v - tail * p.split;
+        tile = p.full_tiles + tail;
+        w.slot = v;
+        const int kb0 = 4 * part * p.part_sb, kb1 = min(p.n_main, kb0 + 4 * p.part_sb);
+        const int zst = part == 0 ? p.n_zst : 0;
+        w.kbase = kb0 - zst;
+        w.n_st = zst + kb1 - kb0;
+    }
+    w.mt = tile % p.m_tiles;
+    w.nt = tile / p.m_tiles;
+    return w;
+}
+
 // ------------------------------------------------------------- producer --
 __device__ __forceinline__ void run_producer(const Ctx& cx, const GemmParams& p, const CUtensorMap* tm_x,
                                              const CUtensorMap* tm_e, const CUtensorMap* tm_d) {
-    const int n_st = p.n_zst + p.n_main;
     int s = 0;
     uint32_t ph = 0, issued = 0, parity_bits = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-        for (int st = 0; st < n_st; ++st) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        const int mt = w.mt, nt = w.nt;
+        for (int st = 0; st < w.n_st; ++st) {
             if (!cx.wait(p, kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
                 ok = false;
                 break;
             }
             const uint32_t fb = cx.bar(kBarFull + s);
-            if (st < p.n_zst) {
+            if (st + w.kbase < 0) {
                 const int j = st / 3, part = st - 3 * j;   // part 0: hi*hi, 1: hi*lo, 2: lo*hi
                 mbar_arrive_expect_tx(fb, kStageA + kStageB);
                 tma_load_3d(cx.a(s), tm_e, fb, 64 * j, 128 * mt, part == 2 ? 1 : 0);
                 tma_load_3d(cx.b(s), tm_d, fb, 64 * j, 128 * nt, part == 1 ? 1 : 0);
             } else {
-                const int kb = st - p.n_zst;
+                const int kb = st + w.kbase;
                 const bool sb_last = (kb & 3) == 3;
                 mbar_arrive_expect_tx(fb, kStageA + kStageNib + kStageSc + kStageDa + (sb_last ? kStageD : 0u));
                 tma_load_2d(cx.a(s), tm_x, fb, 64 * kb, 128 * mt);
@@ -155,30 +190,33 @@ __device__ __forceinline__ void run_producer(const Ctx& cx, const GemmParams& p,
 
 // ----------------------------------------------------------- MMA issuer --
 __device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
-    const int n_st = p.n_zst + p.n_main;
     int s = 0, ab = 0, it = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        const Unit w = unit_of(p, u);
         const int yb = it & 1;
         const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
         if (!cx.wait(p, kBarYEmpty + yb, yph ^ 1u, kSiteMmaYEmpty)) break;
         tc_fence_after();
         const uint32_t ty = cx.tmem + 256u + 128u * yb;
-        for (int st = 0; st < n_st; ++st) {
+        // a unit without min-term stages still completes the buffer's Z phase
+        // (nothing to wait for: the epilogue starts Y at zero itself)
+        if (w.kbase >= 0) tc_commit(cx.bar(kBarZ + yb));
+        for (int st = 0; st < w.n_st; ++st) {
             if (!cx.wait(p, kBarFull + s, ph, kSiteMmaFull)) {
                 ok = false;
                 break;
             }
             const uint64_t ad = sw128_kmajor_desc(cx.a(s));
             const uint64_t bd = sw128_kmajor_desc(cx.b(s));
-            if (st < p.n_zst) {
+            if (st + w.kbase < 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
                     tc_mma_f16(ty, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
                 tc_commit(cx.bar(kBarEmpty + s));
-                if (st == p.n_zst - 1) tc_commit(cx.bar(kBarZ + yb));
+                if (st + w.kbase == -1) tc_commit(cx.bar(kBarZ + yb));
             } else {
                 if (!cx.wait(p, kBarConv + s, ph, kSiteMmaConv)) {
                     ok = false;
@@ -220,7 +258,6 @@ __device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
 // group of 8 consecutive lanes covers 8 consecutive rows: the 16-B reads are
 // contiguous and the granule writes fall in 8 distinct bank quads.
 __device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p, int ci, int lane) {
-    const int n_st = p.n_zst + p.n_main;
     const int r = ci * 32 + lane;
     const uint32_t rx = static_cast<uint32_t>(r & 7);
     const uint32_t row_off = static_cast<uint32_t>(r >> 3) * 1024u + rx * 128u;
@@ -228,13 +265,14 @@ __device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        for (int st = 0; st < n_st; ++st) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        for (int st = 0; st < w.n_st; ++st) {
             if (!cx.warp_wait(p, kBarFull + s, ph, kSiteConvFull)) {
                 ok = false;
                 break;
             }
-            if (st < p.n_zst) {
+            if (st + w.kbase < 0) {
                 // min-term stage: nothing to convert, but arrive anyway so that
                 // every stage barrier completes exactly one phase per ring pass
                 // and the MMA's phase bit stays valid for it
@@ -398,17 +436,33 @@ __device__ __forceinline__ void dump_chunk(const GemmParams& p, int64_t t, int c
 // Warp e (0..7) reads TMEM lanes 32*(warp%4)..+31 (the lane quadrant its
 // warp index allows) and columns 64*(e/4)..+63 of each buffer: each thread
 // owns one token row and 64 output columns.
+// A k-part of a split tile: this warp's 32 x 64 slice of the partial Y (TMEM
+// at ty) to the workspace, for the fixup kernel.  Kept out of line: the
+// epilogue loop's register allocation then stays that of whole tiles.
+__device__ __noinline__ void store_partial(const GemmParams& p, uint32_t ty, int slot, int slice, int lane) {
+    float* dst = p.part + ((static_cast<int64_t>(slot) * 8 + slice) * 32 + lane) * 64;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t Yv[16];
+        tmem_ld16(ty + 16u * q, Yv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            reinterpret_cast<uint4*>(dst + 16 * q)[i] = make_uint4(Yv[4 * i], Yv[4 * i + 1], Yv[4 * i + 2], Yv[4 * i + 3]);
+    }
+}
+
 template <bool kDump, bool kSwiGLU>
 __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p, int warp, int e, int lane) {
-    const int n_st = p.n_zst + p.n_main;
     const int qd = warp & 3, ch = e >> 2;
     const int row = qd * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     int s = 0, ab = 0, it = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-        const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        const Unit w = unit_of(p, u);
+        const int mt = w.mt, nt = w.nt;
         const int yb = it & 1;
         const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
         const uint32_t ty = cx.tmem + lane_off + 256u + 128u * yb + 64u * ch;
@@ -418,13 +472,21 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
 #pragma unroll
         for (int j = 0; j < 64; ++j) P[j] = 0.0f;
         bool zready = false;
-        for (int st = 0; ok && st < n_st; ++st) {
+        if (w.kbase >= 0) {   // no min-term stages write Y: start it at zero
+            uint32_t z[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) z[j] = 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_st16(ty + 16u * q, z);
+            tmem_wait_st();
+        }
+        for (int st = 0; ok && st < w.n_st; ++st) {
             if (!cx.warp_wait(p, kBarFull + s, ph, kSiteEpiFull)) {
                 ok = false;
                 break;
             }
-            if (st >= p.n_zst) {
-                const int kb = st - p.n_zst;
+            const int kb = st + w.kbase;
+            if (kb >= 0) {
                 const float* das = reinterpret_cast<const float*>(cx.sbase + kOffDa + kStageDa * s);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -491,7 +553,12 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
             advance(s, ph);
         }
         if (!ok) break;
-        if constexpr (kSwiGLU) {
+        if (w.slot >= 0) {   // a k-part of a split tile: its partial Y, finished by the fixup kernel
+            store_partial(p, ty, w.slot, qd * 2 + ch, lane);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
+        } else if constexpr (kSwiGLU) {
             // tile done: the 64 columns are 32 gate and 32 up outputs of the
             // down projection's input chunk c = 2 nt + ch
             uint32_t g0[16], g1[16], u0[16], u1[16];
@@ -587,6 +654,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Finishes the k-split tail tiles: one warp per (tail tile, 32 x 64 slice),
+// one thread per token row.  The parts' partial slices are added in part
+// order (the sum does not depend on which part ran where or finished first),
+// then the slice is finished as a whole tile's epilogue would finish it: Y,
+// or with kSwiGLU the down projection's operand of chunk 2 nt + (column half).
+template <bool kSwiGLU>
+__global__ void __launch_bounds__(128) split_fixup_kernel(const GemmParams p) {
+    const int slice = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int tail = slice >> 3, e = slice & 7;   // e = 2 x row quadrant + column half
+    if (tail >= p.num_tiles - p.full_tiles) return;
+    const int tile = p.full_tiles + tail;
+    const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    const int qd = e >> 1, ch = e & 1;
+    const int64_t t = static_cast<int64_t>(mt) * 128 + qd * 32 + lane;
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+    for (int pp = 0; pp < p.split; ++pp) {
+        const float4* src = reinterpret_cast<const float4*>(
+            p.part + ((static_cast<int64_t>(tail * p.split + pp) * 8 + e) * 32 + lane) * 64);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float4 v = src[i];
+            acc[4 * i] += v.x;
+            acc[4 * i + 1] += v.y;
+            acc[4 * i + 2] += v.z;
+            acc[4 * i + 3] += v.w;
+        }
+    }
+    uint32_t v[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[q][j] = __float_as_uint(acc[16 * q + j]);
+    if constexpr (kSwiGLU) {
+        const int c = 2 * nt + ch;
+        if (t < p.m)
+            swiglu_store(p, t, c, v[0], v[1], v[2], v[3]);
+        else   // padding token of the last 128-token tile: scale 0
+            p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = 0.0f;
+    } else if (t < p.m) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) store_row16(p, t, nt * 128 + 64 * ch + 16 * q, v[q]);
+    }
+}
+
 // Bounded-wait self-test: one CTA waits on a barrier nothing completes.
 __global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_cycles) {
     __shared__ __align__(8) uint64_t bar;
@@ -621,6 +734,17 @@ cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const 
         attr_set[dev][variant] = true;
     }
     kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s) {
+    const int slices = (p.num_tiles - p.full_tiles) * 8;
+    if (slices <= 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((slices + 3) / 4);
+    if (p.hq)
+        split_fixup_kernel<true><<<grid, 128, 0, s>>>(p);
+    else
+        split_fixup_kernel<false><<<grid, 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

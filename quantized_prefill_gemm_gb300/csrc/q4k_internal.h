@@ -22,6 +22,11 @@ struct GemmParams {
     int kc, ksb;
     int m_tiles, n_tiles, num_tiles;
     int n_zst, n_main;      // min-term stages and main stages per tile
+    // Work units: tiles [0, full_tiles) whole, then each remaining tile in
+    // `split` parts along k of part_sb super-blocks (part 0 also runs the
+    // min-term stages); split == 1 means every tile is whole.
+    int full_tiles, split, part_sb, num_units;
+    float* part;            // [kMaxSplitUnits][8][32][64] partial tiles (ActLayout)
     int out_bf16;
     // SiLU(gate)*up epilogue (gate/up pair weights, y unused): the down
     // projection's activation operand for kd = n / 2 inputs, in the
@@ -62,6 +67,8 @@ cudaError_t launch_pack_pair(const uint8_t* gate, const uint8_t* up, int64_t n, 
                              cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                         const GemmParams& p, int grid, cudaStream_t s);
+// After a GEMM with split > 1: add each split tile's parts and finish it.
+cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s);
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s);
 

@@ -21,6 +21,9 @@
 //   da   [mp/128][kc][128] f32   d_a (exact f16 value), zero for padding tokens
 //   e    [2][m][kc]        bf16  E = d_a*ssum (exact in fp32) split into
 //                                 hi = bf16(E) (plane 0), lo = bf16(E - hi) (plane 1)
+//   part [kMaxSplitUnits][8][32][64] f32  partial tiles of the GEMM's k-split
+//                                 tail: unit (tail tile, part), slice (2 x row
+//                                 quadrant + column half), row, column
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
@@ -30,6 +33,7 @@ namespace q4k {
 constexpr int64_t kAlign = 1024;
 constexpr int64_t kTileM = 128;   // tokens per GEMM tile (TMEM lanes)
 constexpr int64_t kTileN = 128;   // output features per GEMM tile
+constexpr int64_t kMaxSplitUnits = 160;   // k-split work units of one GEMM launch (>= its grid)
 
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
@@ -48,14 +52,14 @@ struct PackedLayout {
 };
 
 struct ActLayout {
-    int64_t xq, da, e, total;
+    int64_t xq, da, e, part, total;
     ActLayout(int64_t m, int64_t k) {
         const int64_t kc = k / 32, mp = align_up(m, kTileM);
         xq = 0;
         da = align_up(xq + m * k * 2, kAlign);
         e = align_up(da + mp * kc * 4, kAlign);
-        total = align_up(e + 2 * m * kc * 2, kAlign);
-        if (total == 0) total = kAlign;
+        part = align_up(e + 2 * m * kc * 2, kAlign);
+        total = align_up(part + kMaxSplitUnits * 8 * 32 * 64 * 4, kAlign);
     }
 };
 

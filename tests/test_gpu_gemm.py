@@ -164,3 +164,20 @@ def test_repeat_calls_are_identical(q4k):
 def test_bounded_wait_selftest(q4k):
     assert q4k.q4k_selftest_wait_timeout(2_000_000) == q4k.Q4K_ERR_TIMEOUT   # 2 ms limit
     assert q4k.q4k_device_error_word() == 0                                   # reset by the self-test
+
+
+def test_k_split_tail_and_workspace_reuse(q4k):
+    """Tiles left over after the last full wave are split along k into parts
+    whose partial tiles are added by the part that finishes last; the arrival
+    counters live in the workspace and are left at zero.  16 tiles with 8
+    super-blocks each split 8 ways on a 152-SM part: every output against the
+    oracle, three calls on one workspace giving the same bits."""
+    m, n, k = 256, 1024, 2048
+    blocks, x = make_case(n, k, m, "outlier", seed=91)
+    packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+    ws = q4k.q4k_act_quantize(to_dev(x))
+    ys = [q4k.q4k_gemm_quantized(packed, n, k, ws, m, "f32") for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    want, scale = oracle_rows(blocks, x, np.arange(m))
+    assert_close(ys[0].cpu().double().numpy(), want, scale, "f32", "k-split tail")
