@@ -84,7 +84,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     const long long t0 = clock64();
     while (true) {
         if (backoff_ns) __nanosleep(backoff_ns);
-        if (mbar_try_wait(bar, parity)) return true;
+        // sleeps until the phase completes (or the hint passes): a waiting
+        // warp then takes no issue slots from the warps doing work
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort) return false;
         if (static_cast<uint64_t>(clock64() - t0) > timeout) {
             atomicCAS(err, 0u, kErrTimeoutBase | site);
