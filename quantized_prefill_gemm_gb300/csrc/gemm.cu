@@ -654,49 +654,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Finishes the k-split tail tiles: one warp per (tail tile, 32 x 64 slice),
-// one thread per token row.  The parts' partial slices are added in part
-// order (the sum does not depend on which part ran where or finished first),
-// then the slice is finished as a whole tile's epilogue would finish it: Y,
-// or with kSwiGLU the down projection's operand of chunk 2 nt + (column half).
-template <bool kSwiGLU>
-__global__ void __launch_bounds__(128) split_fixup_kernel(const GemmParams p) {
-    const int slice = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    const int tail = slice >> 3, e = slice & 7;   // e = 2 x row quadrant + column half
+// Finishes the k-split tail tiles.  For every element the parts' partial
+// values are added in part order (the sum does not depend on which part ran
+// where or finished first); then the tile is finished as a whole tile's
+// epilogue would finish it.  Work layout: tail tile, slice e (2 x row
+// quadrant + column half, as the GEMM stores them), row r of the slice.
+__device__ __forceinline__ const float* part_row(const GemmParams& p, int tail, int pp, int e, int r) {
+    return p.part + ((static_cast<int64_t>(tail * p.split + pp) * 8 + e) * 32 + r) * 64;
+}
+
+// Y: one thread per 4 consecutive columns of a row (16 per row).
+__global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    const int g = static_cast<int>(gid & 15), r = static_cast<int>((gid >> 4) & 31), e = static_cast<int>((gid >> 9) & 7);
+    const int64_t tail = gid >> 12;
     if (tail >= p.num_tiles - p.full_tiles) return;
-    const int tile = p.full_tiles + tail;
+    const int tile = p.full_tiles + static_cast<int>(tail);
     const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-    const int qd = e >> 1, ch = e & 1;
-    const int64_t t = static_cast<int64_t>(mt) * 128 + qd * 32 + lane;
-    float acc[64];
-#pragma unroll
-    for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+    const int64_t t = static_cast<int64_t>(mt) * 128 + (e >> 1) * 32 + r;
+    if (t >= p.m) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int pp = 0; pp < p.split; ++pp) {
-        const float4* src = reinterpret_cast<const float4*>(
-            p.part + ((static_cast<int64_t>(tail * p.split + pp) * 8 + e) * 32 + lane) * 64);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float4 v = src[i];
-            acc[4 * i] += v.x;
-            acc[4 * i + 1] += v.y;
-            acc[4 * i + 2] += v.z;
-            acc[4 * i + 3] += v.w;
-        }
+        const float4 v = reinterpret_cast<const float4*>(part_row(p, static_cast<int>(tail), pp, e, r))[g];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
     }
-    uint32_t v[4][16];
+    const int64_t col = static_cast<int64_t>(nt) * 128 + 64 * (e & 1) + 4 * g;
+    if (p.out_bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + t * p.ldy + col) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.y) + t * p.ldy + col) = acc;
+    }
+}
+
+// SiLU(gate)*up operand: one warp per row of a slice; lane l adds columns
+// 2l and 2l+1 (gate outputs in lanes 0-15, the matching up outputs in lanes
+// 16-31), then lanes 0-15 form h and quantize the 32-element block with the
+// same operations as the whole-tile epilogue (amax and ssum are exact in any
+// order), so the operand bits are those of an unsplit tile with these sums.
+__global__ void __launch_bounds__(256) split_fixup_swiglu_kernel(const GemmParams p) {
+    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = static_cast<int>(wid & 31), e = static_cast<int>((wid >> 5) & 7);
+    const int64_t tail = wid >> 8;
+    if (tail >= p.num_tiles - p.full_tiles) return;
+    const int tile = p.full_tiles + static_cast<int>(tail);
+    const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    const int64_t t = static_cast<int64_t>(mt) * 128 + (e >> 1) * 32 + r;
+    const int c = 2 * nt + (e & 1);
+    if (t >= p.m) {   // padding token of the last 128-token tile: scale 0
+        if (lane == 0) p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = 0.0f;
+        return;
+    }
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int pp = 0; pp < p.split; ++pp) {
+        const float2 v = reinterpret_cast<const float2*>(part_row(p, static_cast<int>(tail), pp, e, r))[lane];
+        acc.x += v.x;
+        acc.y += v.y;
+    }
+    constexpr unsigned kFull = 0xFFFFFFFFu;
+    const float u0 = __shfl_down_sync(kFull, acc.x, 16), u1 = __shfl_down_sync(kFull, acc.y, 16);
+    const bool gl = lane < 16;
+    const float h0 = gl ? silu_mul_fixed(acc.x, u0) : 0.0f;
+    const float h1 = gl ? silu_mul_fixed(acc.y, u1) : 0.0f;
+    float amax = fmaxf(fabsf(h0), fabsf(h1));
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    amax = __shfl_sync(kFull, amax, 0);
+    const bool live = amax >= 0x1p-120f;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __fdiv_rn(127.0f, amax);
+    int q0 = max(-127, min(127, __float2int_rn(__fmul_rn(h0, inv))));
+    int q1 = max(-127, min(127, __float2int_rn(__fmul_rn(h1, inv))));
+    q0 = (live && gl) ? q0 : 0;
+    q1 = (live && gl) ? q1 : 0;
+    int ssum = q0 + q1;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[q][j] = __float_as_uint(acc[16 * q + j]);
-    if constexpr (kSwiGLU) {
-        const int c = 2 * nt + ch;
-        if (t < p.m)
-            swiglu_store(p, t, c, v[0], v[1], v[2], v[3]);
-        else   // padding token of the last 128-token tile: scale 0
-            p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = 0.0f;
-    } else if (t < p.m) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) store_row16(p, t, nt * 128 + 64 * ch + 16 * q, v[q]);
+    for (int o = 8; o >= 1; o >>= 1) ssum += __shfl_xor_sync(kFull, ssum, o);
+    if (gl) {
+        const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+        const int64_t kd = static_cast<int64_t>(p.hkc) * 32;
+        *reinterpret_cast<__half2*>(p.hq + t * kd + 32 * c + 2 * lane) = pr;
+    }
+    if (lane == 0) {
+        const __half da = __float2half_rn(live ? d : 0.0f);
+        p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = __half2float(da);
+        const float ev = __fmul_rn(__half2float(da), static_cast<float>(ssum));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(ev);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(ev, __bfloat162float(hi)));
+        p.he[t * p.hkc + c] = hi;
+        p.he[(static_cast<int64_t>(p.m) + t) * p.hkc + c] = lo;
     }
 }
 
@@ -738,13 +791,12 @@ cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const 
 }
 
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s) {
-    const int slices = (p.num_tiles - p.full_tiles) * 8;
-    if (slices <= 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>((slices + 3) / 4);
-    if (p.hq)
-        split_fixup_kernel<true><<<grid, 128, 0, s>>>(p);
-    else
-        split_fixup_kernel<false><<<grid, 128, 0, s>>>(p);
+    const int64_t rows = static_cast<int64_t>(p.num_tiles - p.full_tiles) * 8 * 32;   // slice rows
+    if (rows <= 0) return cudaSuccess;
+    if (p.hq)   // a warp per row
+        split_fixup_swiglu_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(p);
+    else        // 16 threads per row
+        split_fixup_kernel<<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
