@@ -7,11 +7,12 @@
 // qa = clamp(rint_half_even(RN32(x*inv)), -127, 127), d_a = RN16(d);
 // blocks with amax < 2^-120 are zero blocks.
 //
-// One 8-lane group per block: each lane loads one float4 (4 consecutive k),
-// the group reduces amax and ssum with shuffles.  Consecutive groups take
-// consecutive blocks of the same token, so a warp reads 512 contiguous bytes.
-// HBM-bound: 4 B read per element, 1 B (public q8) or 2 B (GEMM operand)
-// written per element plus a few bytes per block.
+// One thread per block (q8_rows_kernel, act_quant_kernel): its eight 16-B
+// loads are in flight together and amax and ssum need no shuffles; a warp
+// takes 32 consecutive blocks of one token (4 KB of contiguous fp32).  The
+// q8-to-operand conversion uses an 8-lane group per block.  HBM-bound: 4 B
+// read per element, 1 B (public q8) or 2 B (GEMM operand) written per element
+// plus a few bytes per block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -23,38 +24,42 @@ namespace q4k {
 namespace {
 
 constexpr int kThreadsPerBlock = 256;
-constexpr unsigned kFull = 0xFFFFFFFFu;
 
-struct LaneQ8 {
-    int q[4];
-    int ssum;       // whole block
-    __half da;      // whole block
+// The q8 block of 32 consecutive fp32 values at src (16-byte aligned): codes,
+// d_a and ssum, by the rule in the header of this file (fp32, this order;
+// amax and ssum do not depend on the order of their terms).
+struct BlockQ8 {
+    int q[32];
+    int ssum;
+    __half da;
 };
 
-__device__ __forceinline__ LaneQ8 quantize_lane(float4 v) {
-    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1, 8));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2, 8));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4, 8));
+__device__ __forceinline__ BlockQ8 quantize_block(const float* __restrict__ src) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(src) + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    float amax = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
     const bool live = amax >= 0x1p-120f;
     const float d = __fdiv_rn(amax, 127.0f);
     const float inv = __fdiv_rn(127.0f, amax);
-    LaneQ8 r;
-    const float xs[4] = {v.x, v.y, v.z, v.w};
-    int s = 0;
+    BlockQ8 b;
+    b.ssum = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int q = __float2int_rn(__fmul_rn(xs[i], inv));
-        q = max(-127, min(127, q));
-        r.q[i] = live ? q : 0;
-        s += r.q[i];
+    for (int i = 0; i < 32; ++i) {
+        const int q = max(-127, min(127, __float2int_rn(__fmul_rn(v[i], inv))));
+        b.q[i] = live ? q : 0;
+        b.ssum += b.q[i];
     }
-    s += __shfl_xor_sync(kFull, s, 1, 8);
-    s += __shfl_xor_sync(kFull, s, 2, 8);
-    s += __shfl_xor_sync(kFull, s, 4, 8);
-    r.ssum = s;
-    r.da = __float2half_rn(live ? d : 0.0f);
-    return r;
+    b.da = __float2half_rn(live ? d : 0.0f);
+    return b;
 }
 
 // E = d_a * ssum (exact in fp32: an 11-bit by <= 12-bit product) split into
@@ -75,27 +80,22 @@ __global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_kernel(const float* 
     // one (which may still read q8/da/ssum, or have written x) to finish
     griddep_launch_dependents();
     griddep_wait();
-    const int64_t kc = k / 32;
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t grp = gid >> 3;
-    const int j = static_cast<int>(gid & 7);
-    // whole warps stay in range together: m*kc*8 is a multiple of 8, and a
-    // group's 8 lanes are consecutive, so a warp is either fully in a group
-    // range or its tail groups are all out of range
-    const bool in = grp < m * kc;
-    const int64_t t = in ? grp / kc : 0, c = in ? grp % kc : 0;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (in) v = __ldg(reinterpret_cast<const float4*>(x + t * ldx + c * 32 + 4 * j));
-    const LaneQ8 r = quantize_lane(v);
-    if (!in) return;
-    const uint32_t packed = (static_cast<uint32_t>(r.q[0]) & 0xFFu) | ((static_cast<uint32_t>(r.q[1]) & 0xFFu) << 8) |
-                            ((static_cast<uint32_t>(r.q[2]) & 0xFFu) << 16) |
-                            ((static_cast<uint32_t>(r.q[3]) & 0xFFu) << 24);
-    *reinterpret_cast<uint32_t*>(q8 + t * k + c * 32 + 4 * j) = packed;
-    if (j == 0) {
-        da[t * kc + c] = __half_as_ushort(r.da);
-        ssum[t * kc + c] = static_cast<int16_t>(r.ssum);
-    }
+    const int64_t kc = k / 32, kg = (kc + 31) / 32;   // 32-block groups per token
+    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t t = wid / kg, c = (wid % kg) * 32 + (threadIdx.x & 31);
+    if (t >= m || c >= kc) return;
+    const BlockQ8 b = quantize_block(x + t * ldx + c * 32);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = (static_cast<uint32_t>(b.q[4 * i]) & 0xFFu) | ((static_cast<uint32_t>(b.q[4 * i + 1]) & 0xFFu) << 8) |
+               ((static_cast<uint32_t>(b.q[4 * i + 2]) & 0xFFu) << 16) |
+               ((static_cast<uint32_t>(b.q[4 * i + 3]) & 0xFFu) << 24);
+    uint4* dst = reinterpret_cast<uint4*>(q8 + t * k + c * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    da[t * kc + c] = __half_as_ushort(b.da);
+    ssum[t * kc + c] = static_cast<int16_t>(b.ssum);
 }
 
 __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64_t m, int64_t k, int64_t kc,
@@ -116,28 +116,40 @@ __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64
     }
 }
 
-// GEMM operand form (see q4k_layout.h) from fp32 activations.
+// GEMM operand form (see q4k_layout.h) from fp32 activations.  One thread
+// per 32-k block: its eight 16-B loads are in flight together, amax and ssum
+// need no shuffles, and a warp covers 32 consecutive blocks of one token
+// (4 KB of contiguous fp32 in, 2 KB of fp16 and 64 + 64 B of d_a*ssum out).
 __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float* __restrict__ x, int64_t m,
                                                                      int64_t mp, int64_t k, int64_t ldx,
                                                                      __half* __restrict__ xq,
                                                                      float* __restrict__ dat,
                                                                      __nv_bfloat16* __restrict__ e) {
-    const int64_t kc = k / 32;
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t grp = gid >> 3;
-    const int j = static_cast<int>(gid & 7);
-    const bool in = grp < mp * kc;
-    const int64_t t = in ? grp / kc : 0, c = in ? grp % kc : 0;
-    const bool live_row = in && t < m;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live_row) v = __ldg(reinterpret_cast<const float4*>(x + t * ldx + c * 32 + 4 * j));
-    const LaneQ8 r = quantize_lane(v);
-    if (!in) return;
+    const int64_t kc = k / 32, kg = (kc + 31) / 32;   // 32-block groups per token
+    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = wid / kg, c = (wid % kg) * 32 + lane;
+    if (t >= mp || c >= kc) return;
+    float* da_slot = dat + ((t >> 7) * kc + c) * 128 + (t & 127);
     if (t >= m) {   // padding token of the last 128-token tile: scale 0
-        if (j == 0) dat[((t >> 7) * kc + c) * 128 + (t & 127)] = 0.0f;
+        *da_slot = 0.0f;
         return;
     }
-    write_operand(t, c, j, m, k, kc, r.q, r.da, r.ssum, xq, dat, e);
+    const BlockQ8 b = quantize_block(x + t * ldx + c * 32);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const __half2 pr = __halves2half2(__int2half_rn(b.q[2 * i]), __int2half_rn(b.q[2 * i + 1]));
+        w[i] = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(xq + t * k + c * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    *da_slot = __half2float(b.da);
+    __nv_bfloat16 hi, lo;
+    split_e(b.da, b.ssum, hi, lo);
+    e[t * kc + c] = hi;
+    e[(m + t) * kc + c] = lo;
 }
 
 // GEMM operand form from the public q8 SoA ([m][ldq] int8, da, ssum [m][kc]).
@@ -174,7 +186,7 @@ inline unsigned grid_for(int64_t threads) {
 
 cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8, uint16_t* da,
                                     int16_t* ssum, cudaStream_t s) {
-    const int64_t threads = m * (k / 32) * 8;
+    const int64_t threads = m * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
     if (threads == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_for(threads));
@@ -191,7 +203,7 @@ cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_
 cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s) {
     const ActLayout L(m, k);
     const int64_t mp = align_up(m, kTileM);
-    const int64_t threads = mp * (k / 32) * 8;
+    const int64_t threads = mp * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
     if (threads == 0) return cudaSuccess;
     uint8_t* b = static_cast<uint8_t*>(ws);
     act_quant_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(
