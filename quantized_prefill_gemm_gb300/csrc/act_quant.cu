@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float
                                                                      __half* __restrict__ xq,
                                                                      float* __restrict__ dat,
                                                                      __nv_bfloat16* __restrict__ e) {
+    griddep_launch_dependents();   // programmatic dependent launch (see q8_rows_kernel)
+    griddep_wait();
     const int64_t kc = k / 32, kg = (kc + 31) / 32;   // 32-block groups per token
     const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -160,6 +162,8 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_from_q8_kernel(const int
                                                                        __half* __restrict__ xq,
                                                                        float* __restrict__ dat,
                                                                        __nv_bfloat16* __restrict__ e) {
+    griddep_launch_dependents();   // programmatic dependent launch (see q8_rows_kernel)
+    griddep_wait();
     const int64_t kc = k / 32;
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t grp = gid >> 3;
@@ -188,16 +192,8 @@ cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_
                                     int16_t* ssum, cudaStream_t s) {
     const int64_t threads = m * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
     if (threads == 0) return cudaSuccess;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_for(threads));
-    cfg.blockDim = dim3(kThreadsPerBlock);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, q8_rows_kernel, x, m, k, ldx, q8, da, ssum);
+    return launch_pdl(q8_rows_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, k, ldx, q8, da,
+                      ssum);
 }
 
 cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s) {
@@ -206,10 +202,9 @@ cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ld
     const int64_t threads = mp * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
     if (threads == 0) return cudaSuccess;
     uint8_t* b = static_cast<uint8_t*>(ws);
-    act_quant_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(
-        x, m, mp, k, ldx, reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
-        reinterpret_cast<__nv_bfloat16*>(b + L.e));
-    return cudaGetLastError();
+    return launch_pdl(act_quant_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp, k, ldx,
+                      reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
+                      reinterpret_cast<__nv_bfloat16*>(b + L.e));
 }
 
 cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
@@ -219,10 +214,9 @@ cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16
     const int64_t threads = mp * (k / 32) * 8;
     if (threads == 0) return cudaSuccess;
     uint8_t* b = static_cast<uint8_t*>(ws);
-    act_from_q8_kernel<<<grid_for(threads), kThreadsPerBlock, 0, s>>>(
-        q8, da, ssum, m, mp, k, ldq, reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
-        reinterpret_cast<__nv_bfloat16*>(b + L.e));
-    return cudaGetLastError();
+    return launch_pdl(act_from_q8_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da, ssum, m, mp,
+                      k, ldq, reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
+                      reinterpret_cast<__nv_bfloat16*>(b + L.e));
 }
 
 }  // namespace q4k

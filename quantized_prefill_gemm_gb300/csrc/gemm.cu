@@ -606,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.sbase = smem_raw + (base - raw);
     cx.abort_flag = reinterpret_cast<volatile int*>(cx.sbase + kOffMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -633,6 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.sbase + kOffMisc);
+    // launched with programmatic dependent launch: the set-up above overlaps
+    // the previous kernel's tail; its results (the activation operand) are
+    // read, and Y or the workspace written, only after it has completed
+    griddep_wait();
 
     if (warp == 0) {
         if (lane == 0) run_producer(cx, p, &tm_x, &tm_e, &tm_d);
@@ -665,6 +670,8 @@ __device__ __forceinline__ const float* part_row(const GemmParams& p, int tail, 
 
 // Y: one thread per 4 consecutive columns of a row (16 per row).
 __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
+    griddep_launch_dependents();   // programmatic dependent launch: the GEMM's partials
+    griddep_wait();                // are read only once it has completed
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
     const int g = static_cast<int>(gid & 15), r = static_cast<int>((gid >> 4) & 31), e = static_cast<int>((gid >> 9) & 7);
     const int64_t tail = gid >> 12;
@@ -698,6 +705,8 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
 // same operations as the whole-tile epilogue (amax and ssum are exact in any
 // order), so the operand bits are those of an unsplit tile with these sums.
 __global__ void __launch_bounds__(256) split_fixup_swiglu_kernel(const GemmParams p) {
+    griddep_launch_dependents();   // programmatic dependent launch: the GEMM's partials
+    griddep_wait();                // are read only once it has completed
     const int64_t wid = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int r = static_cast<int>(wid & 31), e = static_cast<int>((wid >> 5) & 7);
@@ -786,18 +795,17 @@ cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const 
         if (e != cudaSuccess) return e;
         attr_set[dev][variant] = true;
     }
-    kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_e, tm_d, p);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, tm_x, tm_e, tm_d, p);
 }
 
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(p.num_tiles - p.full_tiles) * 8 * 32;   // slice rows
     if (rows <= 0) return cudaSuccess;
     if (p.hq)   // a warp per row
-        split_fixup_swiglu_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(p);
-    else        // 16 threads per row
-        split_fixup_kernel<<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0, s>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(split_fixup_swiglu_kernel, dim3(static_cast<unsigned>((rows * 32 + 255) / 256)), dim3(256), 0,
+                          s, p);
+    return launch_pdl(split_fixup_kernel, dim3(static_cast<unsigned>((rows * 16 + 255) / 256)), dim3(256), 0, s,
+                      p);   // 16 threads per row
 }
 
 cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s) {

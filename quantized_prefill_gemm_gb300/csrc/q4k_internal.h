@@ -8,6 +8,25 @@
 
 namespace q4k {
 
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous kernel in the stream finishes; it must execute griddepcontrol.wait
+// before it touches memory that kernel reads or writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct GemmParams {
     const uint8_t* nib;     // packed quants  [nt][kc][128][16 B]
     const uint8_t* sc;      // packed scales  [nt][kc][128]
