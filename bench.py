@@ -245,8 +245,11 @@ def main():
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     achieved = flops_step * args.steps / (gemm_ms * 1e-3) / 1e12
+    # dram__bytes_read.sum + dram__bytes_write.sum of q4k_gemm_kernel per launch, averaged over the 224
+    # launches of one stack step (ncu capture of this kernel version, summarized under profiles/)
+    traffic = 49.35e6 if args.workload == "stack" else None
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "q4k_gemm_kernel",
+                "traffic": traffic, "traffic_unit": "bytes per launch", "kernel": "q4k_gemm_kernel",
                 "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step); the GEMM issues "
                                "f16 tcgen05 MMAs, same rate class",
                 "per_launch": "2*M*N*K algorithmic flops / CUDA-event duration of each GEMM launch"}
