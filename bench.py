@@ -380,10 +380,10 @@ def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
         dist.destroy_process_group()
 
 
-def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2):
-    """Same metric through the public fused call q4k_gemm, with every
-    projection's activations copied from pinned host memory and its result
-    copied back inside the timed region."""
+def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2):
+    """Decode-sized e2e: the copies are a few kB, so they stay on the compute
+    stream (per-projection stream and event bookkeeping would cost more host
+    time than the copies take)."""
     host_x = []
     for x in xs:
         hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -409,10 +409,73 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    h2d = sum(tokens * k * 4 for _, k in mats)
-    d2h = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
-    return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "steps": steps}
+    h2d_bytes = sum(tokens * k * 4 for _, k in mats)
+    d2h_bytes = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
+    return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d_bytes,
+            "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ms, "steps": steps}
+
+
+def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2):
+    """Same metric through the public fused call q4k_gemm, with every
+    projection's activations copied from pinned host memory and its result
+    copied back inside the timed region.  As a serving loop would, the copies
+    run on their own streams (host->device, device->host) with two device
+    buffers per shape, so that projection i+1's input and projection i-1's
+    output move while projection i computes; events order every buffer reuse."""
+    host_x = []
+    for x in xs:
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hx.copy_(x)
+        host_x.append(hx)
+    ydt = torch.bfloat16 if out == "bf16" else torch.float32
+    host_y = [torch.empty((tokens, n), dtype=ydt, pin_memory=True) for n, _ in mats]
+    nbuf = 2
+    dx = {k: [torch.empty((tokens, k), dtype=torch.float32, device=dev) for _ in range(nbuf)] for _, k in mats}
+    dy = {n: [torch.empty((tokens, n), dtype=ydt, device=dev) for _ in range(nbuf)] for n, _ in mats}
+    x_free = {k: [torch.cuda.Event() for _ in range(nbuf)] for k in dx}   # the GEMM that read it is done
+    y_free = {n: [torch.cuda.Event() for _ in range(nbuf)] for n in dy}   # its copy to the host is done
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    uses = {}
+
+    def step():
+        for i, (n, k) in enumerate(mats):
+            bx = uses[("x", k)] = (uses.get(("x", k), -1) + 1) % nbuf
+            by = uses[("y", n)] = (uses.get(("y", n), -1) + 1) % nbuf
+            xb, yb = dx[k][bx], dy[n][by]
+            h2d.wait_event(x_free[k][bx])
+            with torch.cuda.stream(h2d):
+                xb.copy_(host_x[i], non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(h2d)
+            stream.wait_event(arrived)
+            stream.wait_event(y_free[n][by])
+            q4k.q4k_gemm(packed[i], n, k, xb, out_dtype=out, y=yb, workspace=ws, stream=stream)
+            x_free[k][bx].record(stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h.wait_event(done)
+            with torch.cuda.stream(d2h):
+                host_y[i].copy_(yb, non_blocking=True)
+            y_free[n][by].record(d2h)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    h2d.wait_stream(stream)   # the timed copies start after the start marker
+    d2h.wait_stream(stream)
+    for _ in range(steps):
+        step()
+    stream.wait_stream(d2h)
+    stream.wait_stream(h2d)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d_bytes = sum(tokens * k * 4 for _, k in mats)
+    d2h_bytes = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
+    return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d_bytes,
+            "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ms, "steps": steps,
+            "overlap": "copies on their own streams, two device buffers per shape"}
 
 
 def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream):
@@ -505,7 +568,7 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
             "products_ms_per_step": ms_products, "roofline": roofline, "clocks": clk,
             "gpu_launches": (1 if tokens <= 4 else 2) * len(mats) * args.steps}
     if not args.no_e2e and rank == 0:
-        line["e2e"] = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
+        line["e2e"] = run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"], _ = cpu_baseline(args.workload)
     if rank == 0:
