@@ -9,8 +9,9 @@
 //
 // One thread per block (q8_rows_kernel, act_quant_kernel): its eight 16-B
 // loads are in flight together and amax and ssum need no shuffles; a warp
-// takes 32 consecutive blocks of one token (4 KB of contiguous fp32).  The
-// q8-to-operand conversion uses an 8-lane group per block.  HBM-bound: 4 B
+// takes 32 consecutive blocks of one token (4 KB of contiguous fp32).  Small
+// batches of the public q8 form, and the q8-to-operand conversion, use an
+// 8-lane group per block.  HBM-bound: 4 B
 // read per element, 1 B (public q8) or 2 B (GEMM operand) written per element
 // plus a few bytes per block.
 #include <cuda_bf16.h>
@@ -24,6 +25,43 @@ namespace q4k {
 namespace {
 
 constexpr int kThreadsPerBlock = 256;
+
+// An 8-lane group per 32-element block (each lane one float4, amax and ssum
+// by shuffles within the group): eight times the threads of the one-thread
+// form, for batches too small to fill the GPU with one thread per block.
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct LaneQ8 {
+    int q[4];
+    int ssum;       // whole block
+    __half da;      // whole block
+};
+
+__device__ __forceinline__ LaneQ8 quantize_lane(float4 v) {
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4, 8));
+    const bool live = amax >= 0x1p-120f;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __fdiv_rn(127.0f, amax);
+    LaneQ8 r;
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int q = __float2int_rn(__fmul_rn(xs[i], inv));
+        q = max(-127, min(127, q));
+        r.q[i] = live ? q : 0;
+        s += r.q[i];
+    }
+    s += __shfl_xor_sync(kFull, s, 1, 8);
+    s += __shfl_xor_sync(kFull, s, 2, 8);
+    s += __shfl_xor_sync(kFull, s, 4, 8);
+    r.ssum = s;
+    r.da = __float2half_rn(live ? d : 0.0f);
+    return r;
+}
 
 // The q8 block of 32 consecutive fp32 values at src (16-byte aligned): codes,
 // d_a and ssum, by the rule in the header of this file (fp32, this order;
@@ -68,6 +106,35 @@ __device__ __forceinline__ void split_e(__half da, int ssum, __nv_bfloat16& hi, 
     const float e = __fmul_rn(__half2float(da), static_cast<float>(ssum));
     hi = __float2bfloat16_rn(e);
     lo = __float2bfloat16_rn(__fsub_rn(e, __bfloat162float(hi)));
+}
+
+// Public SoA output, 8-lane groups (small batches).
+__global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_lanes_kernel(const float* __restrict__ x, int64_t m,
+                                                                         int64_t k, int64_t ldx,
+                                                                         int8_t* __restrict__ q8,
+                                                                         uint16_t* __restrict__ da,
+                                                                         int16_t* __restrict__ ssum) {
+    griddep_launch_dependents();   // programmatic dependent launch (see q8_rows_kernel)
+    griddep_wait();
+    const int64_t kc = k / 32;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t grp = gid >> 3;
+    const int j = static_cast<int>(gid & 7);
+    // whole 8-lane groups stay in range together: m*kc*8 is a multiple of 8
+    const bool in = grp < m * kc;
+    const int64_t t = in ? grp / kc : 0, c = in ? grp % kc : 0;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (in) v = __ldg(reinterpret_cast<const float4*>(x + t * ldx + c * 32 + 4 * j));
+    const LaneQ8 r = quantize_lane(v);
+    if (!in) return;
+    const uint32_t packed = (static_cast<uint32_t>(r.q[0]) & 0xFFu) | ((static_cast<uint32_t>(r.q[1]) & 0xFFu) << 8) |
+                            ((static_cast<uint32_t>(r.q[2]) & 0xFFu) << 16) |
+                            ((static_cast<uint32_t>(r.q[3]) & 0xFFu) << 24);
+    *reinterpret_cast<uint32_t*>(q8 + t * k + c * 32 + 4 * j) = packed;
+    if (j == 0) {
+        da[t * kc + c] = __half_as_ushort(r.da);
+        ssum[t * kc + c] = static_cast<int16_t>(r.ssum);
+    }
 }
 
 // Public SoA output: q8 [m][k], da f16 [m][kc], ssum i16 [m][kc].
@@ -190,8 +257,13 @@ inline unsigned grid_for(int64_t threads) {
 
 cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8, uint16_t* da,
                                     int16_t* ssum, cudaStream_t s) {
+    const int64_t blocks = m * (k / 32);
+    if (blocks == 0) return cudaSuccess;
+    // fewer blocks than about 64 CTAs of one thread each: 8 lanes per block
+    if (blocks < 64 * kThreadsPerBlock)
+        return launch_pdl(q8_rows_lanes_kernel, dim3(grid_for(blocks * 8)), dim3(kThreadsPerBlock), 0, s, x, m, k, ldx,
+                          q8, da, ssum);
     const int64_t threads = m * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
-    if (threads == 0) return cudaSuccess;
     return launch_pdl(q8_rows_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, k, ldx, q8, da,
                       ssum);
 }

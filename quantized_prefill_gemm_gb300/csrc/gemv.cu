@@ -32,6 +32,7 @@
 // Z[t] += (d_a[t] * ssum[t]) * (-dmin * m) (both factors exact in fp32); per
 // super-block Y[t] += d * P[t].
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cuda_fp16.h>
 
 #include "q4k_internal.h"
@@ -43,6 +44,7 @@ namespace {
 constexpr int kRows = 16;      // od rows per CTA
 constexpr int kParts = 16;     // super-block shares per row (2 per warp)
 constexpr int kThreads = 256;
+constexpr size_t kPersistMaxSmem = 220 * 1024;   // persistent form: activations + partial sums
 
 // 4-bit quants of one 8-k group (one packed word) -> two words of 4 bytes in
 // k order.  In the packed word the nibble at bits 4j is k = 2j and the nibble
@@ -259,6 +261,231 @@ __global__ void __launch_bounds__(kThreads, kQuant ? 2 : 1) q4k_gemv_kernel(cons
     }
 }
 
+// ------------------------------------------------------- persistent form --
+// The same arithmetic with the activations staged once per CTA: the grid is
+// one or two CTAs per SM, each CTA first copies (q8 input) or quantizes (fp32
+// input) all m x k activations into shared memory, then walks 16-row groups
+// g = blockIdx.x, blockIdx.x + gridDim.x, ...  A thread's weights for the
+// next (row group, super-block) are in flight while it computes the current
+// one, across row-group boundaries too, so the weight stream does not stop
+// between groups.  Per group the 16 shares of a row are added in shared
+// memory in a fixed order, as above.
+struct PersistSmem {
+    size_t act, da, ss, red, total;   // byte offsets: q8 [m][k], d_a f16 [m][kc], ssum [m][kc], partial sums
+    __host__ __device__ static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
+    __host__ __device__ PersistSmem(int mslots, int k) {
+        const size_t kc = static_cast<size_t>(k) / 32;
+        act = 0;
+        da = a16(static_cast<size_t>(mslots) * k);
+        ss = da + a16(static_cast<size_t>(mslots) * kc * 2);
+        red = ss + a16(static_cast<size_t>(mslots) * kc * 2);
+        total = red + static_cast<size_t>(kParts) * mslots * kRows * 4;
+    }
+};
+
+// One 32-element q8 block quantized by one thread (the rule of the activation
+// quantizer: d = RN(amax/127), inv = RN(127/amax), qa = clamp(rint_even(
+// RN(x*inv)), -127, 127), d_a = RN16(d), zero block below 2^-120).
+__device__ __forceinline__ void quantize_block_to(const float* __restrict__ src, int8_t* dst, uint16_t* da,
+                                                  int16_t* ss) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(src) + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    float amax = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const bool live = amax >= 0x1p-120f;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __fdiv_rn(127.0f, amax);
+    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        int q = max(-127, min(127, __float2int_rn(__fmul_rn(v[i], inv))));
+        q = live ? q : 0;
+        s += q;
+        w[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
+    }
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    *da = __half_as_ushort(__float2half_rn(live ? d : 0.0f));
+    *ss = static_cast<int16_t>(s);
+}
+
+template <int M, bool kQuant>
+__global__ void __launch_bounds__(kThreads, M == 1 ? 2 : 1) q4k_gemv_persistent_kernel(const GemvParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hl = lane & 15;
+    const int part = 2 * warp + (lane >> 4);
+    const int kc = p.kc, ksb = p.ksb, m = p.m, k = p.k;
+    const int groups = p.n / kRows;
+    const PersistSmem L(M, k);
+    int8_t* act = reinterpret_cast<int8_t*>(smem_raw + L.act);
+    uint16_t* sda = reinterpret_cast<uint16_t*>(smem_raw + L.da);
+    int16_t* sss = reinterpret_cast<int16_t*>(smem_raw + L.ss);
+    float* red = reinterpret_cast<float*>(smem_raw + L.red);
+
+    // programmatic dependent launch: this CTA's first row group streams into
+    // L2 while the previous kernel finishes
+    griddep_launch_dependents();
+    if (blockIdx.x < groups) {
+        const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRows;
+        const int64_t tile0 = row0 >> 7, r0 = row0 & 127;
+        for (int c = threadIdx.x; c < kc; c += kThreads)
+            prefetch_l2(p.nib + ((tile0 * kc + c) * 128 + r0) * 16, kRows * 16);
+    }
+    griddep_wait();
+
+    // the first weights are requested before the activations are staged
+    const int rounds = (ksb + kParts - 1) / kParts;
+    SbWeights cur, nxt;
+    int g = blockIdx.x;
+    if (g < groups && part < ksb) {
+        const int64_t o = static_cast<int64_t>(g) * kRows + hl;
+        load_weights(p, o >> 7, o & 127, part, cur);
+    }
+    if constexpr (kQuant) {
+        for (int i = threadIdx.x; i < m * kc; i += kThreads) {
+            const int t = i / kc, c = i - t * kc;
+            quantize_block_to(p.xf + static_cast<int64_t>(t) * p.ldx + 32 * c, act + static_cast<int64_t>(t) * k + 32 * c,
+                              sda + t * kc + c, sss + t * kc + c);
+        }
+    } else {
+        const int v16 = k / 16, s8 = kc / 8;   // 16-B pieces of a q8 row and of a scale row
+        for (int i = threadIdx.x; i < m * v16; i += kThreads) {
+            const int t = i / v16, j = i - t * v16;
+            reinterpret_cast<int4*>(act + static_cast<int64_t>(t) * k)[j] =
+                __ldg(reinterpret_cast<const int4*>(p.q8 + t * p.ldq) + j);
+        }
+        for (int i = threadIdx.x; i < m * s8; i += kThreads) {
+            const int t = i / s8, j = i - t * s8;
+            reinterpret_cast<uint4*>(sda + t * kc)[j] = __ldg(reinterpret_cast<const uint4*>(p.da + t * kc) + j);
+            reinterpret_cast<uint4*>(sss + t * kc)[j] = __ldg(reinterpret_cast<const uint4*>(p.ssum + t * kc) + j);
+        }
+    }
+    __syncthreads();
+
+    for (; g < groups; g += gridDim.x) {
+        const int64_t o = static_cast<int64_t>(g) * kRows + hl;
+        const int64_t nt = o >> 7, r = o & 127;
+        const int gn = g + gridDim.x;   // this CTA's next row group
+        float acc[M];
+#pragma unroll
+        for (int t = 0; t < M; ++t) acc[t] = 0.0f;
+        for (int round = 0; round < rounds; ++round) {
+            const int sb = part + round * kParts;
+            if (sb >= ksb) continue;   // no barrier inside the round: nothing to keep in step
+            if (sb + kParts < ksb) {
+                load_weights(p, nt, r, sb + kParts, nxt);
+            } else if (gn < groups) {
+                const int64_t on = static_cast<int64_t>(gn) * kRows + hl;
+                load_weights(p, on >> 7, on & 127, part, nxt);
+            }
+            const int64_t srec = (nt * ksb + sb) * 128 + r;
+            const float d = __ldg(p.dsb + srec);
+            const float dmin = __ldg(p.dmn + srec);
+            float P[M], Z[M];
+#pragma unroll
+            for (int t = 0; t < M; ++t) {
+                P[t] = 0.0f;
+                Z[t] = 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t q[8];
+                unpack_group(cur.q[j].x, q[0], q[1]);
+                unpack_group(cur.q[j].y, q[2], q[3]);
+                unpack_group(cur.q[j].z, q[4], q[5]);
+                unpack_group(cur.q[j].w, q[6], q[7]);
+                const int sc = static_cast<int>(cur.scm[j] & 0xFFu);
+                const float nm = -(dmin * static_cast<float>(cur.scm[j] >> 8));   // exact: f16 value x 6-bit m
+                const int c = 8 * sb + j;
+#pragma unroll
+                for (int t = 0; t < M; ++t) {
+                    if (t < m) {
+                        const int4* a = reinterpret_cast<const int4*>(act + static_cast<int64_t>(t) * k + 32 * c);
+                        const int4 a0 = a[0], a1 = a[1];
+                        int J = __dp4a(static_cast<int>(q[0]), a0.x, 0);
+                        J = __dp4a(static_cast<int>(q[1]), a0.y, J);
+                        J = __dp4a(static_cast<int>(q[2]), a0.z, J);
+                        J = __dp4a(static_cast<int>(q[3]), a0.w, J);
+                        J = __dp4a(static_cast<int>(q[4]), a1.x, J);
+                        J = __dp4a(static_cast<int>(q[5]), a1.y, J);
+                        J = __dp4a(static_cast<int>(q[6]), a1.z, J);
+                        J = __dp4a(static_cast<int>(q[7]), a1.w, J);
+                        const float da = __half2float(__ushort_as_half(sda[t * kc + c]));
+                        const float ss = static_cast<float>(sss[t * kc + c]);
+                        P[t] = fmaf(da, static_cast<float>(sc * J), P[t]);
+                        Z[t] = fmaf(da * ss, nm, Z[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < M; ++t) acc[t] = fmaf(d, P[t], acc[t]) + Z[t];
+            cur = nxt;
+        }
+        // add the 16 shares of each row in a fixed order
+        __syncthreads();   // the previous group's sums have been read
+#pragma unroll
+        for (int t = 0; t < M; ++t) red[(part * M + t) * kRows + hl] = acc[t];
+        __syncthreads();
+        for (int i = threadIdx.x; i < M * kRows; i += kThreads) {
+            const int t = i / kRows, rr = i % kRows;
+            if (t >= m) continue;
+            float v = 0.0f;
+#pragma unroll
+            for (int s2 = 0; s2 < kParts; ++s2) v += red[(s2 * M + t) * kRows + rr];
+            const int64_t oo = static_cast<int64_t>(g) * kRows + rr;
+            if (p.out_bf16)
+                static_cast<__nv_bfloat16*>(p.y)[t * p.ldy + oo] = __float2bfloat16_rn(v);
+            else
+                static_cast<float*>(p.y)[t * p.ldy + oo] = v;
+        }
+    }
+}
+
+// Launch the persistent form when its activations fit in shared memory and
+// there are enough row groups; otherwise leave *launched false.
+template <int M, bool kQuant>
+cudaError_t launch_gemv_persistent(const GemvParams& p, cudaStream_t s, bool* launched) {
+    *launched = false;
+    static size_t smem_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const size_t smem = PersistSmem(M, p.k).total;
+    if (smem > kPersistMaxSmem) return cudaSuccess;   // too large: the caller uses the other form
+    if (smem_set[dev] < smem) {   // raise the kernel's dynamic shared memory limit once per size class
+        e = cudaFuncSetAttribute(q4k_gemv_persistent_kernel<M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPersistMaxSmem));
+        if (e != cudaSuccess) return e;
+        smem_set[dev] = kPersistMaxSmem;
+    }
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q4k_gemv_persistent_kernel<M, kQuant>, kThreads,
+                                                          smem)) != cudaSuccess)
+        return e;
+    const int groups = static_cast<int>(p.n / kRows);
+    const int slots = std::max(1, per_sm) * sms;
+    // Staging all activations pays off only when a CTA then works through
+    // several row groups (measured: with one group per CTA the per-group form
+    // is faster); quantizing them costs more than copying, so it needs more.
+    if (groups <= (kQuant ? 2 : 1) * slots) return cudaSuccess;
+    const int grid = std::min(groups, slots);
+    *launched = true;
+    return launch_pdl(q4k_gemv_persistent_kernel<M, kQuant>, dim3(grid), dim3(kThreads), smem, s, p);
+}
+
 template <int M, bool kQuant>
 cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
     static bool attr_set[64] = {};
@@ -285,12 +512,20 @@ cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<M, kQuant>, p);
 }
 
+template <int M, bool kQuant>
+cudaError_t launch_gemv_any(const GemvParams& p, cudaStream_t s) {
+    bool launched = false;
+    const cudaError_t e = launch_gemv_persistent<M, kQuant>(p, s, &launched);
+    if (e != cudaSuccess || launched) return e;
+    return launch_gemv_m<M, kQuant>(p, s);
+}
+
 cudaError_t launch_gemv_q8(const GemvParams& p, cudaStream_t s) {
-    if (p.m <= 1) return launch_gemv_m<1, false>(p, s);
-    if (p.m <= 2) return launch_gemv_m<2, false>(p, s);
-    if (p.m <= 4) return launch_gemv_m<4, false>(p, s);
-    if (p.m <= 8) return launch_gemv_m<8, false>(p, s);
-    return launch_gemv_m<16, false>(p, s);
+    if (p.m <= 1) return launch_gemv_any<1, false>(p, s);
+    if (p.m <= 2) return launch_gemv_any<2, false>(p, s);
+    if (p.m <= 4) return launch_gemv_any<4, false>(p, s);
+    if (p.m <= 8) return launch_gemv_any<8, false>(p, s);
+    return launch_gemv_any<16, false>(p, s);
 }
 
 }  // namespace
@@ -298,9 +533,9 @@ cudaError_t launch_gemv_q8(const GemvParams& p, cudaStream_t s) {
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
     if (!p.xf) return launch_gemv_q8(p, s);
     // in-kernel quantization is built for up to 4 tokens (the caller's limit)
-    if (p.m <= 1) return launch_gemv_m<1, true>(p, s);
-    if (p.m <= 2) return launch_gemv_m<2, true>(p, s);
-    if (p.m <= 4) return launch_gemv_m<4, true>(p, s);
+    if (p.m <= 1) return launch_gemv_any<1, true>(p, s);
+    if (p.m <= 2) return launch_gemv_any<2, true>(p, s);
+    if (p.m <= 4) return launch_gemv_any<4, true>(p, s);
     return cudaErrorInvalidValue;
 }
 

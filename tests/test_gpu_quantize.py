@@ -49,6 +49,22 @@ def test_q8_edge_blocks(q4k):
     _check(q4k, x)
 
 
+def test_q8_edge_blocks_large_batch(q4k):
+    """The same special rows in a batch large enough (19,200 blocks) for the
+    one-thread-per-block kernel (small batches use 8 lanes per block)."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((600, 1024)).astype(np.float32)
+    x[0::6] = 0.0
+    x[1::6, :32] = np.float32(2.0 ** -121)
+    x[1::6, 32:64] = np.float32(2.0 ** -119)
+    x[2::6] = rng.integers(-127, 128, (100, 1024)).astype(np.float32)
+    x[2::6, ::32] = 127.0
+    x[3::6] = np.float32(0.5) * (np.arange(1024, dtype=np.float32) % 256) - 64.0
+    x[4::6] *= 1e4
+    x[5::6] *= 1e-6
+    _check(q4k, x)
+
+
 def test_q8_strided_rows(q4k):
     from quantized_prefill_gemm_gb300 import inputs
 
