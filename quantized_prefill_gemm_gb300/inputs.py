@@ -4,7 +4,8 @@ This module only draws random numbers; it holds none of the GEMM's
 arithmetic, so both the CUDA path and the CPU oracle can consume what it
 makes without sharing any of the method.
 
-Weights are random Q4_K super-blocks of 144 bytes per 256 weights.  Bytes 0-1
+Weights are random Q4_K super-blocks of 144 bytes per 256 weights (Q6_K:
+210 bytes, see q6k_blocks).  Bytes 0-1
 and 2-3 are the little-endian f16 words d and dmin, each drawn uniform on
 [1e-3, 1e-2] and rounded to f16.  The other 140 bytes (sub-block scales and
 mins, then the 4-bit quants) are uniform random bytes: in the Q4_K layout every
@@ -52,6 +53,24 @@ def q4k_blocks(n: int, k: int, seed: int, tag: int = 0) -> np.ndarray:
     return blocks
 
 
+Q6K_BLOCK_BYTES = 210
+Q6K_D_LO, Q6K_D_HI = 1e-4, 1e-3
+
+
+def q6k_blocks(n: int, k: int, seed: int, tag: int = 0) -> np.ndarray:
+    """Random Q6_K weights, shape [n][k/256][210] uint8: uniform bytes for the
+    quant bits and the int8 sub-block scales (so q ~ U{0..63}, sc ~ U{-128..127}),
+    bytes 208-209 the f16 d ~ U[1e-4, 1e-3]."""
+    if k % QK_K:
+        raise ValueError("k must be a multiple of 256")
+    rng = _rng(seed, 3000 + tag)
+    nb = k // QK_K
+    blocks = rng.integers(0, 256, size=(n, nb, Q6K_BLOCK_BYTES), dtype=np.uint8)
+    d = rng.uniform(Q6K_D_LO, Q6K_D_HI, size=(n, nb, 1)).astype(np.float16)
+    blocks[:, :, 208:210] = d.view(np.uint8).reshape(n, nb, 2)
+    return blocks
+
+
 def activations(m: int, k: int, seed: int, kind: str = "normal", tag: int = 0) -> np.ndarray:
     """Random fp32 activations, shape [m][k] row-major."""
     rng = _rng(seed, 2000 + tag)
@@ -92,6 +111,19 @@ def q4k_blocks_torch(n: int, k: int, seed: int, tag: int = 0, device="cuda"):
     blocks = torch.randint(0, 256, (n, nb, BLOCK_BYTES), generator=g, device=device, dtype=torch.uint8)
     u = torch.empty((n, nb, 2), device=device, dtype=torch.float32).uniform_(D_LO, D_HI, generator=g)
     blocks[:, :, 0:4] = u.to(torch.float16).view(torch.uint8).reshape(n, nb, 4)
+    return blocks
+
+
+def q6k_blocks_torch(n: int, k: int, seed: int, tag: int = 0, device="cuda"):
+    import torch
+
+    if k % QK_K:
+        raise ValueError("k must be a multiple of 256")
+    g = _torch_gen(seed, 3000 + tag, device)
+    nb = k // QK_K
+    blocks = torch.randint(0, 256, (n, nb, Q6K_BLOCK_BYTES), generator=g, device=device, dtype=torch.uint8)
+    u = torch.empty((n, nb, 1), device=device, dtype=torch.float32).uniform_(Q6K_D_LO, Q6K_D_HI, generator=g)
+    blocks[:, :, 208:210] = u.to(torch.float16).view(torch.uint8).reshape(n, nb, 2)
     return blocks
 
 
