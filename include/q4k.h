@@ -207,6 +207,36 @@ q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t
                                      void* h_ws, size_t h_ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Q6_K weights (decode sizes).  The series moves on from Q4_K to a Q6_K line
+ * ("34 · r31 — q-major sda scale-read repack", §5 Results, post-hoc notes);
+ * the pages give no layout for it.  Blocks follow the public GGUF Q6_K
+ * format: 256 weights in 210 bytes (ql[128] low 4 bits, qh[64] high 2 bits,
+ * sc[16] signed 8-bit scales of 16 weights each, d f16 at bytes 208-209),
+ * w = d * sc * (q - 32).
+ * q6k_pack_weights  blocks [n][k/256] x 210 B (device) -> packed
+ *            (q6k_packed_bytes(n, k) bytes, 256-byte aligned).
+ * q6k_gemm   as q4k_gemm (same arguments, activation forms and accuracy
+ *            contract) for 1 <= m <= Q4K_SMALL_M tokens: per 32-k block the
+ *            exact integer sum_s sc_s * sum (q - 32) * qa (two 16-weight
+ *            sub-blocks), then d_a * d times it.  With f32 input and
+ *            m <= Q4K_FUSED_QUANT_M the kernel quantizes the activations
+ *            itself (workspace unused); for larger m the q8 SoA goes to the
+ *            start of `workspace` (q4k_gemm_workspace_bytes(m, n, k, act)).
+ *            Larger m (and activations too large for the kernel's shared
+ *            memory: m x k bytes plus scales, at most ~200 KB) return
+ *            Q4K_ERR_SHAPE: the tensor-core path covers Q4_K only.
+ * n % 128 == 0, k % 256 == 0.
+ * ------------------------------------------------------------------------ */
+size_t q6k_packed_bytes(int64_t n, int64_t k);
+q4k_status q6k_pack_weights(const void* q6k_blocks, int64_t n, int64_t k,
+                            void* packed, size_t packed_bytes, cudaStream_t stream);
+q4k_status q6k_gemm(const void* packed_w, int64_t n, int64_t k,
+                    int act, const void* x_or_q8, const void* da_f16, const void* ssum,
+                    int64_t m, int64_t ldx,
+                    void* y, int out_dtype, int64_t ldy,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * q4k_gemm_static_workspace -- q4k_gemm without a workspace argument.
  * Library addition with no counterpart in the pages: it exists for callers
  * that cannot hand the library scratch memory, e.g. a plain C host that holds

@@ -467,6 +467,87 @@ q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t
                     stream);
 }
 
+size_t q6k_packed_bytes(int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0 || n % kTileN || k % 256 || n >= kMaxDim || k >= kMaxDim) return 0;
+    return static_cast<size_t>(Q6Layout(n, k).total);
+}
+
+q4k_status q6k_pack_weights(const void* blocks, int64_t n, int64_t k, void* packed, size_t packed_bytes,
+                            cudaStream_t stream) {
+    if (n <= 0 || k <= 0 || n % kTileN || k % 256 || n >= kMaxDim || k >= kMaxDim) return Q4K_ERR_SHAPE;
+    if (!blocks || !packed) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(packed, 256)) return Q4K_ERR_ALIGNMENT;
+    if (packed_bytes < q6k_packed_bytes(n, k)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    return from_cuda(launch_pack_q6k(static_cast<const uint8_t*>(blocks), n, k, static_cast<uint8_t*>(packed), stream));
+}
+
+q4k_status q6k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const void* x_or_q8, const void* da_f16,
+                    const void* ssum, int64_t m, int64_t ldx, void* y, int out_dtype, int64_t ldy, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+    q4k_status st = check_gemm_shape(n, k, m);
+    if (st != Q4K_OK) return st;
+    if ((st = check_output(y, m, n, out_dtype, ldy)) != Q4K_OK) return st;
+    if (!packed_w) return Q4K_ERR_INVALID_ARG;
+    if (act != Q4K_ACT_F32 && act != Q4K_ACT_Q8) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(packed_w, 256)) return Q4K_ERR_ALIGNMENT;
+    if (m == 0) return Q4K_OK;
+    if (m > Q4K_SMALL_M || !gemv_q6k_fits(static_cast<int>(m), k)) return Q4K_ERR_SHAPE;   // decode sizes only
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != Q4K_OK) return st;
+    const Q6Layout W(n, k);
+    const uint8_t* wb = static_cast<const uint8_t*>(packed_w);
+    GemvParams g;
+    std::memset(&g, 0, sizeof(g));
+    g.nib = wb + W.lo;
+    g.q6hi = wb + W.hi;
+    g.sc = wb + W.sc;
+    g.dsb = reinterpret_cast<const float*>(wb + W.dsb);
+    g.q6 = 1;
+    g.y = y;
+    g.ldy = ldy;
+    g.m = static_cast<int>(m);
+    g.n = static_cast<int>(n);
+    g.k = static_cast<int>(k);
+    g.kc = static_cast<int>(k / 32);
+    g.ksb = static_cast<int>(k / 256);
+    g.out_bf16 = out_dtype == Q4K_OUT_BF16 ? 1 : 0;
+    if (act == Q4K_ACT_F32) {
+        const float* xf = static_cast<const float*>(x_or_q8);
+        if ((st = check_act_f32(xf, m, k, ldx)) != Q4K_OK) return st;
+        if (m <= kFusedQuantMaxM) {   // one launch: the kernel quantizes the activations itself
+            g.xf = xf;
+            g.ldx = ldx;
+            return from_cuda(launch_gemv_q6k(g, stream));
+        }
+        const SmallMLayout L(m, k);
+        if (!workspace) return Q4K_ERR_INVALID_ARG;
+        if (!aligned(workspace, 256)) return Q4K_ERR_ALIGNMENT;
+        if (workspace_bytes < static_cast<size_t>(L.total)) return Q4K_ERR_WORKSPACE;
+        uint8_t* wsb = static_cast<uint8_t*>(workspace);
+        int8_t* q8 = reinterpret_cast<int8_t*>(wsb + L.q8);
+        uint16_t* da = reinterpret_cast<uint16_t*>(wsb + L.da);
+        int16_t* ss = reinterpret_cast<int16_t*>(wsb + L.ssum);
+        if ((st = q8_quantize_rows(xf, m, k, ldx, q8, da, ss, stream)) != Q4K_OK) return st;
+        g.q8 = q8;
+        g.da = da;
+        g.ssum = ss;
+        g.ldq = k;
+        return from_cuda(launch_gemv_q6k(g, stream));
+    }
+    const int8_t* q8 = static_cast<const int8_t*>(x_or_q8);
+    if (!q8 || !da_f16 || !ssum) return Q4K_ERR_INVALID_ARG;
+    if (ldx < k) return Q4K_ERR_SHAPE;
+    if (!aligned(q8, 16) || ldx % 16 || !aligned(da_f16, 16) || !aligned(ssum, 16)) return Q4K_ERR_ALIGNMENT;
+    g.q8 = q8;
+    g.da = static_cast<const uint16_t*>(da_f16);
+    g.ssum = static_cast<const int16_t*>(ssum);
+    g.ldq = ldx;
+    return from_cuda(launch_gemv_q6k(g, stream));
+}
+
 unsigned int q4k_device_error_word(int reset) {
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != Q4K_OK) return 0xFFFFFFFFu;

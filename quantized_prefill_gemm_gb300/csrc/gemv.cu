@@ -318,6 +318,54 @@ __device__ __forceinline__ void quantize_block_to(const float* __restrict__ src,
     *ss = static_cast<int16_t>(s);
 }
 
+// Stage all m x k activations of the call in shared memory: copy the q8 SoA
+// (16-byte pieces), or quantize fp32 rows one 32-element block per thread.
+template <bool kQuant>
+__device__ __forceinline__ void stage_activations(const GemvParams& p, int8_t* act, uint16_t* sda, int16_t* sss) {
+    const int kc = p.kc, m = p.m, k = p.k;
+    if constexpr (kQuant) {
+        for (int i = threadIdx.x; i < m * kc; i += kThreads) {
+            const int t = i / kc, c = i - t * kc;
+            quantize_block_to(p.xf + static_cast<int64_t>(t) * p.ldx + 32 * c, act + static_cast<int64_t>(t) * k + 32 * c,
+                              sda + t * kc + c, sss + t * kc + c);
+        }
+    } else {
+        const int v16 = k / 16, s8 = kc / 8;   // 16-B pieces of a q8 row and of a scale row
+        for (int i = threadIdx.x; i < m * v16; i += kThreads) {
+            const int t = i / v16, j = i - t * v16;
+            reinterpret_cast<int4*>(act + static_cast<int64_t>(t) * k)[j] =
+                __ldg(reinterpret_cast<const int4*>(p.q8 + t * p.ldq) + j);
+        }
+        for (int i = threadIdx.x; i < m * s8; i += kThreads) {
+            const int t = i / s8, j = i - t * s8;
+            reinterpret_cast<uint4*>(sda + t * kc)[j] = __ldg(reinterpret_cast<const uint4*>(p.da + t * kc) + j);
+            reinterpret_cast<uint4*>(sss + t * kc)[j] = __ldg(reinterpret_cast<const uint4*>(p.ssum + t * kc) + j);
+        }
+    }
+}
+
+// Add the 16 shares of each row of group g in a fixed order and store them.
+template <int M>
+__device__ __forceinline__ void reduce_store(const GemvParams& p, float* red, const float (&acc)[M], int part, int hl,
+                                             int g) {
+    __syncthreads();   // the previous group's sums have been read
+#pragma unroll
+    for (int t = 0; t < M; ++t) red[(part * M + t) * kRows + hl] = acc[t];
+    __syncthreads();
+    for (int i = threadIdx.x; i < M * kRows; i += kThreads) {
+        const int t = i / kRows, rr = i % kRows;
+        if (t >= p.m) continue;
+        float v = 0.0f;
+#pragma unroll
+        for (int s2 = 0; s2 < kParts; ++s2) v += red[(s2 * M + t) * kRows + rr];
+        const int64_t oo = static_cast<int64_t>(g) * kRows + rr;
+        if (p.out_bf16)
+            static_cast<__nv_bfloat16*>(p.y)[t * p.ldy + oo] = __float2bfloat16_rn(v);
+        else
+            static_cast<float*>(p.y)[t * p.ldy + oo] = v;
+    }
+}
+
 template <int M, bool kQuant>
 __global__ void __launch_bounds__(kThreads, M == 1 ? 2 : 1) q4k_gemv_persistent_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -351,25 +399,7 @@ __global__ void __launch_bounds__(kThreads, M == 1 ? 2 : 1) q4k_gemv_persistent_
         const int64_t o = static_cast<int64_t>(g) * kRows + hl;
         load_weights(p, o >> 7, o & 127, part, cur);
     }
-    if constexpr (kQuant) {
-        for (int i = threadIdx.x; i < m * kc; i += kThreads) {
-            const int t = i / kc, c = i - t * kc;
-            quantize_block_to(p.xf + static_cast<int64_t>(t) * p.ldx + 32 * c, act + static_cast<int64_t>(t) * k + 32 * c,
-                              sda + t * kc + c, sss + t * kc + c);
-        }
-    } else {
-        const int v16 = k / 16, s8 = kc / 8;   // 16-B pieces of a q8 row and of a scale row
-        for (int i = threadIdx.x; i < m * v16; i += kThreads) {
-            const int t = i / v16, j = i - t * v16;
-            reinterpret_cast<int4*>(act + static_cast<int64_t>(t) * k)[j] =
-                __ldg(reinterpret_cast<const int4*>(p.q8 + t * p.ldq) + j);
-        }
-        for (int i = threadIdx.x; i < m * s8; i += kThreads) {
-            const int t = i / s8, j = i - t * s8;
-            reinterpret_cast<uint4*>(sda + t * kc)[j] = __ldg(reinterpret_cast<const uint4*>(p.da + t * kc) + j);
-            reinterpret_cast<uint4*>(sss + t * kc)[j] = __ldg(reinterpret_cast<const uint4*>(p.ssum + t * kc) + j);
-        }
-    }
+    stage_activations<kQuant>(p, act, sda, sss);
     __syncthreads();
 
     for (; g < groups; g += gridDim.x) {
@@ -431,24 +461,158 @@ __global__ void __launch_bounds__(kThreads, M == 1 ? 2 : 1) q4k_gemv_persistent_
             for (int t = 0; t < M; ++t) acc[t] = fmaf(d, P[t], acc[t]) + Z[t];
             cur = nxt;
         }
-        // add the 16 shares of each row in a fixed order
-        __syncthreads();   // the previous group's sums have been read
+        reduce_store<M>(p, red, acc, part, hl, g);
+    }
+}
+
+// --------------------------------------------------------------- Q6_K --
+// Q6_K weights (w = d*sc*(q-32), one signed 8-bit sc per 16 weights) in the
+// persistent form.  Per 32-k chunk the exact integer
+//   I = sc_0 * sum_{k<16} (q-32)*qa + sc_1 * sum_{k>=16} (q-32)*qa
+// (|I| <= 32*128*32*127 < 2^24, exact in fp32), then P += d_a*I per chunk
+// and Y += d*P per super-block.  The packed 6-bit u = q ^ 32 is q - 32 in
+// 6-bit two's complement: low nibbles and the 2 high bits are put back into
+// bytes and sign-extended, and dp4a multiplies signed bytes.
+struct SbWeightsQ6 {
+    uint4 lo[8];
+    uint2 hi[8];
+    uint32_t sc[8];   // the chunk's two i8 scales (bytes 0 and 1)
+};
+
+__device__ __forceinline__ void load_weights_q6(const GemvParams& p, int64_t nt, int64_t r, int sb, SbWeightsQ6& w) {
+    const int64_t rec0 = (nt * p.kc + 8 * sb) * 128 + r;
 #pragma unroll
-        for (int t = 0; t < M; ++t) red[(part * M + t) * kRows + hl] = acc[t];
-        __syncthreads();
-        for (int i = threadIdx.x; i < M * kRows; i += kThreads) {
-            const int t = i / kRows, rr = i % kRows;
-            if (t >= m) continue;
-            float v = 0.0f;
-#pragma unroll
-            for (int s2 = 0; s2 < kParts; ++s2) v += red[(s2 * M + t) * kRows + rr];
-            const int64_t oo = static_cast<int64_t>(g) * kRows + rr;
-            if (p.out_bf16)
-                static_cast<__nv_bfloat16*>(p.y)[t * p.ldy + oo] = __float2bfloat16_rn(v);
-            else
-                static_cast<float*>(p.y)[t * p.ldy + oo] = v;
+    for (int j = 0; j < 8; ++j) {
+        w.lo[j] = __ldg(reinterpret_cast<const uint4*>(p.nib) + rec0 + 128 * j);
+        w.hi[j] = __ldg(reinterpret_cast<const uint2*>(p.q6hi) + rec0 + 128 * j);
+        w.sc[j] = __ldg(reinterpret_cast<const uint16_t*>(p.sc) + rec0 + 128 * j);
+    }
+}
+
+// Signed bytes q - 32 of 8-k group g: lo word, and the hi word shifted to the group.
+__device__ __forceinline__ void unpack_q6(uint32_t lo, uint32_t hi, uint32_t& v0123, uint32_t& v4567) {
+    uint32_t l0, l1, h0, h1;
+    unpack_group(lo, l0, l1);
+    unpack_group(hi & 0x33333333u, h0, h1);
+    const uint32_t u0 = l0 | (h0 << 4), u1 = l1 | (h1 << 4);   // 6-bit u per byte
+    v0123 = u0 | ((u0 & 0x20202020u) * 6u);                     // copy bit 5 into bits 6 and 7
+    v4567 = u1 | ((u1 & 0x20202020u) * 6u);
+}
+
+template <int M, bool kQuant>
+__global__ void __launch_bounds__(kThreads, 1) q6k_gemv_persistent_kernel(const GemvParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hl = lane & 15;
+    const int part = 2 * warp + (lane >> 4);
+    const int kc = p.kc, ksb = p.ksb, m = p.m, k = p.k;
+    const int groups = p.n / kRows;
+    const PersistSmem L(M, k);
+    int8_t* act = reinterpret_cast<int8_t*>(smem_raw + L.act);
+    uint16_t* sda = reinterpret_cast<uint16_t*>(smem_raw + L.da);
+    int16_t* sss = reinterpret_cast<int16_t*>(smem_raw + L.ss);
+    float* red = reinterpret_cast<float*>(smem_raw + L.red);
+
+    griddep_launch_dependents();
+    if (blockIdx.x < groups) {
+        const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRows;
+        const int64_t tile0 = row0 >> 7, r0 = row0 & 127;
+        for (int c = threadIdx.x; c < kc; c += kThreads) {
+            prefetch_l2(p.nib + ((tile0 * kc + c) * 128 + r0) * 16, kRows * 16);
+            prefetch_l2(p.q6hi + ((tile0 * kc + c) * 128 + r0) * 8, kRows * 8);
         }
     }
+    griddep_wait();
+
+    const int rounds = (ksb + kParts - 1) / kParts;
+    SbWeightsQ6 cur, nxt;
+    int g = blockIdx.x;
+    if (g < groups && part < ksb) {
+        const int64_t o = static_cast<int64_t>(g) * kRows + hl;
+        load_weights_q6(p, o >> 7, o & 127, part, cur);
+    }
+    stage_activations<kQuant>(p, act, sda, sss);
+    __syncthreads();
+
+    for (; g < groups; g += gridDim.x) {
+        const int64_t o = static_cast<int64_t>(g) * kRows + hl;
+        const int64_t nt = o >> 7, r = o & 127;
+        const int gn = g + gridDim.x;
+        float acc[M];
+#pragma unroll
+        for (int t = 0; t < M; ++t) acc[t] = 0.0f;
+        for (int round = 0; round < rounds; ++round) {
+            const int sb = part + round * kParts;
+            if (sb >= ksb) continue;
+            if (sb + kParts < ksb) {
+                load_weights_q6(p, nt, r, sb + kParts, nxt);
+            } else if (gn < groups) {
+                const int64_t on = static_cast<int64_t>(gn) * kRows + hl;
+                load_weights_q6(p, on >> 7, on & 127, part, nxt);
+            }
+            const float d = __ldg(p.dsb + (nt * ksb + sb) * 128 + r);
+            float P[M];
+#pragma unroll
+            for (int t = 0; t < M; ++t) P[t] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t v[8];
+                unpack_q6(cur.lo[j].x, cur.hi[j].x, v[0], v[1]);
+                unpack_q6(cur.lo[j].y, cur.hi[j].x >> 2, v[2], v[3]);
+                unpack_q6(cur.lo[j].z, cur.hi[j].y, v[4], v[5]);
+                unpack_q6(cur.lo[j].w, cur.hi[j].y >> 2, v[6], v[7]);
+                const int sc0 = static_cast<int>(static_cast<int8_t>(cur.sc[j] & 0xFFu));
+                const int sc1 = static_cast<int>(static_cast<int8_t>((cur.sc[j] >> 8) & 0xFFu));
+                const int c = 8 * sb + j;
+#pragma unroll
+                for (int t = 0; t < M; ++t) {
+                    if (t < m) {
+                        const int4* a = reinterpret_cast<const int4*>(act + static_cast<int64_t>(t) * k + 32 * c);
+                        const int4 a0 = a[0], a1 = a[1];
+                        int J0 = __dp4a(static_cast<int>(v[0]), a0.x, 0);
+                        J0 = __dp4a(static_cast<int>(v[1]), a0.y, J0);
+                        J0 = __dp4a(static_cast<int>(v[2]), a0.z, J0);
+                        J0 = __dp4a(static_cast<int>(v[3]), a0.w, J0);
+                        int J1 = __dp4a(static_cast<int>(v[4]), a1.x, 0);
+                        J1 = __dp4a(static_cast<int>(v[5]), a1.y, J1);
+                        J1 = __dp4a(static_cast<int>(v[6]), a1.z, J1);
+                        J1 = __dp4a(static_cast<int>(v[7]), a1.w, J1);
+                        const float da = __half2float(__ushort_as_half(sda[t * kc + c]));
+                        P[t] = fmaf(da, static_cast<float>(sc0 * J0 + sc1 * J1), P[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < M; ++t) acc[t] = fmaf(d, P[t], acc[t]);
+            cur = nxt;
+        }
+        reduce_store<M>(p, red, acc, part, hl, g);
+    }
+}
+
+template <int M, bool kQuant>
+cudaError_t launch_q6k_gemv_m(const GemvParams& p, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const size_t smem = PersistSmem(M, p.k).total;
+    if (smem > kPersistMaxSmem) return cudaErrorInvalidValue;   // the caller checks the size first
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(q6k_gemv_persistent_kernel<M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPersistMaxSmem));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q6k_gemv_persistent_kernel<M, kQuant>, kThreads,
+                                                          smem)) != cudaSuccess)
+        return e;
+    const int groups = static_cast<int>(p.n / kRows);
+    const int grid = std::max(1, std::min(groups, std::max(1, per_sm) * sms));
+    return launch_pdl(q6k_gemv_persistent_kernel<M, kQuant>, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
 // Launch the persistent form when its activations fit in shared memory and
@@ -529,6 +693,25 @@ cudaError_t launch_gemv_q8(const GemvParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool gemv_q6k_fits(int m, int64_t k) {
+    const int slots = m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;   // the kernel's token slots
+    return PersistSmem(slots, static_cast<int>(k)).total <= kPersistMaxSmem;
+}
+
+cudaError_t launch_gemv_q6k(const GemvParams& p, cudaStream_t s) {
+    if (p.xf) {   // in-kernel quantization: up to 4 tokens (the caller's limit)
+        if (p.m <= 1) return launch_q6k_gemv_m<1, true>(p, s);
+        if (p.m <= 2) return launch_q6k_gemv_m<2, true>(p, s);
+        if (p.m <= 4) return launch_q6k_gemv_m<4, true>(p, s);
+        return cudaErrorInvalidValue;
+    }
+    if (p.m <= 1) return launch_q6k_gemv_m<1, false>(p, s);
+    if (p.m <= 2) return launch_q6k_gemv_m<2, false>(p, s);
+    if (p.m <= 4) return launch_q6k_gemv_m<4, false>(p, s);
+    if (p.m <= 8) return launch_q6k_gemv_m<8, false>(p, s);
+    return launch_q6k_gemv_m<16, false>(p, s);
+}
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
     if (!p.xf) return launch_gemv_q8(p, s);

@@ -108,7 +108,64 @@ __global__ void __launch_bounds__(kThreadsPerBlock) pack_kernel(const uint8_t* _
     dmn[(nt * ksb + sb) * 128 + r] = dmin;
 }
 
+// Q6_K (q6k_blocks layout of the public GGUF format: ql[128], qh[64],
+// sc[16] int8, d f16; w = d*sc*(q-32)) -> Q6Layout.  One thread per (row,
+// super-block).
+__global__ void __launch_bounds__(kThreadsPerBlock) pack_q6k_kernel(const uint8_t* __restrict__ blocks, int64_t n,
+                                                                    int64_t k, uint8_t* __restrict__ packed,
+                                                                    int64_t off_hi, int64_t off_sc, int64_t off_dsb) {
+    const int64_t ksb = k / 256, kc = k / 32;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= n * ksb) return;
+    const int64_t o = idx / ksb, sb = idx % ksb;
+    const uint8_t* blk = blocks + idx * 210;
+    const int64_t nt = o >> 7, r = o & 127;
+    for (int j = 0; j < 8; ++j) {   // chunk c = 8 sb + j: weights 32j .. 32j+31 of the super-block
+        uint8_t u[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int wi = 32 * j + i;                 // weight index in the super-block
+            const int h = wi >> 7, l = wi & 31, part = (wi >> 5) & 3;
+            const uint8_t lob = blk[64 * h + l + ((part & 1) ? 32 : 0)];
+            const uint8_t hib = blk[128 + 32 * h + l];
+            const int q = (((part & 2) ? (lob >> 4) : (lob & 15)) | (((hib >> (2 * part)) & 3) << 4));
+            u[i] = static_cast<uint8_t>(q ^ 32);
+        }
+        uint32_t lw[4], hw[2] = {0u, 0u};
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {   // 8-k group g: k = 8g .. 8g+7 of the chunk
+            uint32_t w = 0;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t ue = u[8 * g + 2 * jj], uo = u[8 * g + 2 * jj + 1];
+                w |= (ue & 15u) << (4 * jj);
+                w |= (uo & 15u) << (16 + 4 * jj);
+                hw[g >> 1] |= ((ue >> 4) & 3u) << (4 * jj + 2 * (g & 1));
+                hw[g >> 1] |= ((uo >> 4) & 3u) << (16 + 4 * jj + 2 * (g & 1));
+            }
+            lw[g] = w;
+        }
+        const int64_t rec = (nt * kc + sb * 8 + j) * 128 + r;
+        *reinterpret_cast<uint4*>(packed + rec * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        *reinterpret_cast<uint2*>(packed + off_hi + rec * 8) = make_uint2(hw[0], hw[1]);
+        packed[off_sc + rec * 2] = blk[192 + 2 * j];
+        packed[off_sc + rec * 2 + 1] = blk[192 + 2 * j + 1];
+    }
+    const float d = __half2float(__ushort_as_half(
+        static_cast<unsigned short>(blk[208] | (static_cast<unsigned>(blk[209]) << 8))));
+    reinterpret_cast<float*>(packed + off_dsb)[(nt * ksb + sb) * 128 + r] = d;
+}
+
 }  // namespace
+
+cudaError_t launch_pack_q6k(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s) {
+    const Q6Layout L(n, k);
+    const int64_t threads = n * (k / 256);
+    if (threads == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((threads + kThreadsPerBlock - 1) / kThreadsPerBlock);
+    pack_q6k_kernel<<<grid, kThreadsPerBlock, 0, s>>>(blocks, n, k, packed, L.hi, L.sc, L.dsb);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s) {
     const PackedLayout L(n, k);

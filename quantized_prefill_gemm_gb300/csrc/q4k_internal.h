@@ -69,6 +69,10 @@ struct GemvParams {
     const uint16_t* da;      // f16 bits [m][kc]
     const int16_t* ssum;     // [m][kc]
     const float* xf;         // fp32 activations [m][ldx]; when set, quantized in the kernel (q8/da/ssum unused)
+    // Q6_K weights (Q6Layout) instead of Q4_K: nib = lo, sc = the i8 scale
+    // pairs, dsb = d; mq and dmn unused
+    const uint8_t* q6hi;
+    int q6;
     void* y;                 // [m][ldy]
     int64_t ldq, ldx, ldy;
     int m, n, k, kc, ksb;
@@ -81,6 +85,8 @@ cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ld
 cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
                                int64_t ldq, void* ws, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
+// Q6_K blocks [n][k/256] x 210 B -> Q6Layout (small-M path)
+cudaError_t launch_pack_q6k(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
 // gate and up [n][k/256] blocks each -> one packed matrix of 2n interleaved rows
 cudaError_t launch_pack_pair(const uint8_t* gate, const uint8_t* up, int64_t n, int64_t k, uint8_t* packed,
                              cudaStream_t s);
@@ -89,6 +95,10 @@ cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const 
 // After a GEMM with split > 1: add each split tile's parts and finish it.
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s);
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
+// Q6_K small-M product (p.q6 set); gemv_q6k_fits says whether m tokens of k
+// activations fit its shared memory
+bool gemv_q6k_fits(int m, int64_t k);
+cudaError_t launch_gemv_q6k(const GemvParams& p, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s);
 
 }  // namespace q4k

@@ -51,6 +51,28 @@ struct PackedLayout {
     }
 };
 
+// Q6_K weights for the small-M path (q6k_pack_weights -> q6k_gemm), for n
+// rows and k inputs, nt = n/128, kc = k/32, ksb = k/256.  With u = q ^ 32 (the
+// 6-bit two's complement of q - 32):
+//   lo  [nt][kc][128][16 B]  low 4 bits of u, nibbles arranged as in nib above
+//   hi  [nt][kc][128][8 B]   bits 4-5 of u: word 0 holds 8-k groups 0 and 1,
+//                             word 1 groups 2 and 3; the group's 2-bit fields
+//                             sit at the group's nibble positions (first group
+//                             of the word in bits 0-1, second in bits 2-3)
+//   sc  [nt][kc][128][2]  i8  the scales of the chunk's two 16-weight sub-blocks
+//   dsb [nt][ksb][128]    f32 super-block scale d
+struct Q6Layout {
+    int64_t lo, hi, sc, dsb, total;
+    Q6Layout(int64_t n, int64_t k) {
+        const int64_t kc = k / 32, ksb = k / 256;
+        lo = 0;
+        hi = align_up(lo + n * k / 2, kAlign);
+        sc = align_up(hi + n * k / 4, kAlign);
+        dsb = align_up(sc + n * kc * 2, kAlign);
+        total = align_up(dsb + n * ksb * 4, kAlign);
+    }
+};
+
 struct ActLayout {
     int64_t xq, da, e, part, total;
     ActLayout(int64_t m, int64_t k) {

@@ -51,6 +51,10 @@ SIGNATURES = {
                                  _c_ptr, _c_size, _c_ptr, _c_size, _c_ptr]),
     "q4k_gemm_swiglu_quantized": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_size,
                                            _c_ptr]),
+    "q6k_packed_bytes": (_c_size, [_c_i64, _c_i64]),
+    "q6k_pack_weights": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_ptr]),
+    "q6k_gemm": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
+                          _c_ptr, _c_int, _c_i64, _c_ptr, _c_size, _c_ptr]),
     "q4k_static_workspace_bytes": (_c_size, []),
     "q4k_gemm_static_workspace": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
                                            _c_ptr, _c_int, _c_i64, _c_ptr]),
@@ -254,6 +258,43 @@ def q4k_gemm_swiglu_quantized(packed: torch.Tensor, n: int, k: int, workspace: t
         _dev(packed, "packed"), n, k, _dev(workspace, "workspace"), workspace.numel(), m, _dev(h_ws, "h_ws"),
         h_ws.numel(), _stream(stream)))
     return h_ws
+
+
+def q6k_packed_bytes(n: int, k: int) -> int:
+    return int(LIB.q6k_packed_bytes(n, k))
+
+
+def q6k_pack_weights(blocks: torch.Tensor, n: int, k: int, packed=None, stream=None) -> torch.Tensor:
+    """Q6_K blocks (uint8 [n][k/256][210] on the GPU) -> packed uint8 buffer."""
+    size = q6k_packed_bytes(n, k)
+    if size == 0:
+        raise ValueError("unsupported weight shape (n % 128, k % 256)")
+    if blocks.numel() != n * (k // 256) * 210 or not blocks.is_contiguous():
+        raise ValueError("blocks must be contiguous [n][k/256][210] uint8")
+    packed = torch.empty(size, dtype=torch.uint8, device=blocks.device) if packed is None else packed
+    _check("q6k_pack_weights", LIB.q6k_pack_weights(
+        _dev(blocks, "blocks", torch.uint8), n, k, _dev(packed, "packed", torch.uint8), packed.numel(),
+        _stream(stream)))
+    return packed
+
+
+def q6k_gemm(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, out_dtype="f32", da=None, ssum=None,
+             y=None, workspace=None, stream=None) -> torch.Tensor:
+    """Y[m][n] = x @ W^T for Q6_K weights, 1 <= m <= 16 tokens."""
+    m, kx, ldx = _row_major(x, "x")
+    if kx != k:
+        raise ValueError("x has the wrong number of columns")
+    act = ACT_Q8 if x.dtype == torch.int8 else ACT_F32
+    if act == ACT_Q8 and (da is None or ssum is None):
+        raise ValueError("q8 input needs da and ssum")
+    code, y, ldy = _out(m, n, out_dtype, y, x.device)
+    workspace = _workspace(q4k_gemm_workspace_bytes(m, n, k, act), x.device, workspace)
+    _check("q6k_gemm", LIB.q6k_gemm(
+        _dev(packed, "packed"), n, k, act, _dev(x, "x"),
+        _dev(da, "da", torch.float16) if act == ACT_Q8 else None,
+        _dev(ssum, "ssum", torch.int16) if act == ACT_Q8 else None,
+        m, ldx, _dev(y, "y"), code, ldy, _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return y
 
 
 def q4k_static_workspace_bytes() -> int:

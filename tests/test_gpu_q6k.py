@@ -1,0 +1,88 @@
+"""q6k_gemm (Q6_K weights, decode sizes) on the GPU vs the oracle.
+
+Bar as for Q4_K: per element |y_gpu - y_oracle| <= 1e-4 * sum_k |w_k * a_k|
+(plus one bf16 rounding for bf16 output); fp32 activations quantized inside
+the kernel must give the bits of the same kernel fed the quantizer's q8.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import q6k_blocks as oq6
+from oracle import q8 as oq8
+from quantized_prefill_gemm_gb300 import inputs
+from tests.gpu_common import DEV, assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q4k():
+    from quantized_prefill_gemm_gb300 import q4k as mod
+
+    mod.q4k_device_error_word(reset=True)
+    yield mod
+    assert mod.q4k_device_error_word() == 0
+
+
+def _oracle(blocks, x):
+    f = oq6.decode(blocks)
+    qa, da, _ = oq8.quantize_rows(x)
+    return oq6.gemm_blockwise(f, qa, da), oq6.abs_scale(f, qa, da)
+
+
+def _check(q4k, n, k, m, seed, out="f32", act="f32", kind="normal"):
+    blocks = inputs.q6k_blocks(n, k, seed)
+    x = inputs.activations(m, k, seed, kind)
+    packed = q4k.q6k_pack_weights(to_dev(blocks), n, k)
+    if act == "q8":
+        q, da, ss = q4k.q8_quantize_rows(to_dev(x))
+        y = q4k.q6k_gemm(packed, n, k, q, out_dtype=out, da=da, ssum=ss)
+    else:
+        y = q4k.q6k_gemm(packed, n, k, to_dev(x), out_dtype=out)
+    torch.cuda.synchronize()
+    want, scale = _oracle(blocks, x)
+    assert_close(y.float().cpu().double().numpy(), want, scale, out, f"q6k {m}x{n}x{k} {act} {out}")
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 8, 13, 16])
+def test_token_counts(q4k, m):
+    _check(q4k, 256, 512, m, 10 + m)
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+def test_q8_input_bf16(q4k, m):
+    _check(q4k, 384, 768, m, 30 + m, out="bf16", act="q8", kind="outlier")
+
+
+@pytest.mark.parametrize("n,k,m,out", [(4096, 4096, 1, "bf16"), (11008, 4096, 4, "bf16"), (4096, 11008, 16, "f32")])
+def test_decode_sizes(q4k, n, k, m, out):
+    """7B projection shapes (every output checked; 11008 rows give the
+    persistent CTAs several row groups each)."""
+    _check(q4k, n, k, m, 50 + m, out=out, kind="silu_mul" if k == 11008 else "normal")
+
+
+@pytest.mark.parametrize("m", [1, 3, 4])
+def test_in_kernel_quantization_bits(q4k, m):
+    n, k = 512, 2816
+    blocks = inputs.q6k_blocks(n, k, 70 + m)
+    x = inputs.activations(m, k, 70 + m, "outlier")
+    packed = q4k.q6k_pack_weights(to_dev(blocks), n, k)
+    xd = to_dev(x)
+    a = q4k.q6k_gemm(packed, n, k, xd)
+    q, da, ss = q4k.q8_quantize_rows(xd)
+    b = q4k.q6k_gemm(packed, n, k, q, da=da, ssum=ss)
+    c = q4k.q6k_gemm(packed, n, k, xd)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_rejects_prefill_sizes(q4k):
+    n, k = 256, 512
+    packed = q4k.q6k_pack_weights(to_dev(inputs.q6k_blocks(n, k, 1)), n, k)
+    with pytest.raises(q4k.Q4KError):
+        q4k.q6k_gemm(packed, n, k, torch.zeros((17, k), dtype=torch.float32, device=DEV))
+    big = 14336
+    packed = q4k.q6k_pack_weights(to_dev(inputs.q6k_blocks(n, big, 1)), n, big)
+    with pytest.raises(q4k.Q4KError):   # 16 x 14336 activations do not fit the kernel's shared memory
+        q4k.q6k_gemm(packed, n, big, torch.zeros((16, big), dtype=torch.float32, device=DEV))
