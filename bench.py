@@ -53,6 +53,10 @@ WORKLOADS = {
                "7B linear stack at decode size: 32 layers x {q,k,v,o 4096x4096; gate,up 11008x4096; down "
                "4096x11008} Q4_K, 1 token, fused q8 activation quantization, bf16 out (small-M path, "
                "CUDA-graph replay)"),
+    "decode_q6k": (1, [(n, k) for _ in range(32) for (_, n, k) in LAYER], "bf16",
+                   "7B linear stack at decode size with Q6_K weights (5.31 GB): 32 layers x {q,k,v,o 4096x4096; "
+                   "gate,up 11008x4096; down 4096x11008}, 1 token, fused q8 activation quantization, bf16 out "
+                   "(Q6_K small-M path, CUDA-graph replay)"),
     "decode_gate": (1, [(11008, 4096)], "bf16",
                     "7B FFN gate projection 11008x4096 Q4_K at decode size: 1 token, fused q8, bf16 out "
                     "(small-M path, CUDA-graph replay)"),
@@ -186,9 +190,14 @@ def main():
     kind = "outlier" if args.workload == "qproj2630" else "normal"
     # weights (packed once, resident) and one activation matrix per projection
     packed, xs, ys = [], [], []
+    q6 = args.workload == "decode_q6k"
     for i, (n, k) in enumerate(mats):
-        blocks = inputs.q4k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
-        packed.append(q4k.q4k_pack_weights(blocks, n, k))
+        if q6:
+            blocks = inputs.q6k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
+            packed.append(q4k.q6k_pack_weights(blocks, n, k))
+        else:
+            blocks = inputs.q4k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
+            packed.append(q4k.q4k_pack_weights(blocks, n, k))
         del blocks
         kind_i = "silu_mul" if (args.workload == "ffn" and i == 2) else kind
         xs.append(inputs.activations_torch(tokens, k, seed=4 + rank, kind=kind_i, tag=i, device=dev))
@@ -380,7 +389,7 @@ def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
         dist.destroy_process_group()
 
 
-def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2):
+def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2, gemm=None):
     """Decode-sized e2e: the copies are a few kB, so they stay on the compute
     stream (per-projection stream and event bookkeeping would cost more host
     time than the copies take)."""
@@ -397,7 +406,7 @@ def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, s
     def step():
         for i, (n, k) in enumerate(mats):
             dx[k].copy_(host_x[i], non_blocking=True)
-            q4k.q4k_gemm(packed[i], n, k, dx[k], out_dtype=out, y=dy[n], workspace=ws, stream=stream)
+            (gemm or q4k.q4k_gemm)(packed[i], n, k, dx[k], out_dtype=out, y=dy[n], workspace=ws, stream=stream)
             host_y[i].copy_(dy[n], non_blocking=True)
 
     step()
@@ -488,16 +497,19 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
     Q4_K weights at 144 B / 256 + the q8 input (1 B per element + 4 B per 32)
     + the bf16 output, against the measured HBM copy bandwidth."""
     tokens, out = WORKLOADS[args.workload][0], WORKLOADS[args.workload][2]
+    q6 = args.workload == "decode_q6k"
+    gemm = q4k.q6k_gemm if q6 else q4k.q4k_gemm
+    wbytes = 210 if q6 else 144   # per 256 weights
     q8s = [q4k.q8_quantize_rows(x) for x in xs]
 
     def fused():
         for i, (n, k) in enumerate(mats):
-            q4k.q4k_gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws)
+            gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws)
 
     def products():
         for i, (n, k) in enumerate(mats):
             q, da, ss = q8s[i]
-            q4k.q4k_gemm(packed[i], n, k, q, out_dtype=out, da=da, ssum=ss, y=ys[i], workspace=ws)
+            gemm(packed[i], n, k, q, out_dtype=out, da=da, ssum=ss, y=ys[i], workspace=ws)
 
     side = torch.cuda.Stream(device=dev)
     graphs = {}
@@ -544,17 +556,17 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
     if err:
         raise RuntimeError(f"device error word 0x{err:x}")
 
-    bytes_step = sum(n * k * 144 / 256 + tokens * (k + k // 32 * 4) + tokens * n * 2 for n, k in mats)
-    weights_gb = sum(n * k * 144 / 256 for n, k in mats) / 1e9
+    bytes_step = sum(n * k * wbytes / 256 + tokens * (k + k // 32 * 4) + tokens * n * 2 for n, k in mats)
+    weights_gb = sum(n * k * wbytes / 256 for n, k in mats) / 1e9
     peaks, src = load_peaks()
     peak = float(peaks["hbm_gbs"])
     achieved = bytes_step / (ms_products * 1e-3) / 1e9
     flops_step = sum(2.0 * tokens * n * k for n, k in mats)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "q4k_gemv_kernel",
+                "traffic": None, "kernel": "q6k_gemv_persistent_kernel" if q6 else "q4k_gemv_kernel",
                 "peak_source": f"{src} HBM copy bandwidth",
-                "per_launch": "algorithmic bytes (Q4_K weights 144 B/256 + q8 input + bf16 output) / "
-                              "graph-replayed duration of the 224 small-M products, per launch"}
+                "per_launch": f"algorithmic bytes ({'Q6_K' if q6 else 'Q4_K'} weights {wbytes} B/256 + q8 input + "
+                              "bf16 output) / graph-replayed duration of the 224 small-M products, per launch"}
     desc = WORKLOADS[args.workload][3]
     line = {"metric": METRIC, "value": world * tokens / (ms_step * 1e-3), "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -568,7 +580,7 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
             "products_ms_per_step": ms_products, "roofline": roofline, "clocks": clk,
             "gpu_launches": (1 if tokens <= 4 else 2) * len(mats) * args.steps}
     if not args.no_e2e and rank == 0:
-        line["e2e"] = run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
+        line["e2e"] = run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, gemm=gemm)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"], _ = cpu_baseline(args.workload)
     if rank == 0:

@@ -500,7 +500,7 @@ __device__ __forceinline__ void unpack_q6(uint32_t lo, uint32_t hi, uint32_t& v0
 }
 
 template <int M, bool kQuant>
-__global__ void __launch_bounds__(kThreads, 1) q6k_gemv_persistent_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kThreads, M == 1 ? 2 : 1) q6k_gemv_persistent_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hl = lane & 15;
