@@ -283,11 +283,19 @@ q4k_status q4k_gemm_static_workspace(const void* packed_w, int64_t n, int64_t k,
  *                        sum_{k in chunk c} (sc*q)[o,k]*qa[t,k] (exact
  *                        integers) to chunk_acc [m][n][k/32]; test hook,
  *                        limited to m*n*(k/32) <= 2^26.  Asynchronous.
+ * q6k_gemm_debug_chunk_acc  the same for Q6_K weights on the tensor-core
+ *                        path: J[t][o][c] = sum_s sc_s * sum (q - 32) * qa
+ *                        over the chunk's two sub-blocks; workspace holds the
+ *                        bf16 operand form (from q6k_gemm's own quantization,
+ *                        i.e. a prior q6k_gemm call with m > 16 on it).
  * ------------------------------------------------------------------------ */
 unsigned int q4k_device_error_word(int reset);
 q4k_status q4k_device_status(int reset);
 q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
 q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k,
+                                    void* workspace, size_t workspace_bytes, int64_t m,
+                                    float* y, int64_t ldy, float* chunk_acc, cudaStream_t stream);
+q4k_status q6k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k,
                                     void* workspace, size_t workspace_bytes, int64_t m,
                                     float* y, int64_t ldy, float* chunk_acc, cudaStream_t stream);
 

@@ -136,9 +136,10 @@ q4k_status check_output(const void* y, int64_t m, int64_t n, int out, int64_t ld
 
 // h_ws (gate/up pair weights only): instead of Y, write the down projection's
 // operand of SiLU(gate)*up, ActLayout(m, n / 2), there; y, out and ldy are then
-// unused.  The caller has checked h_ws.
+// unused.  The caller has checked h_ws.  q6: Q6_K weights (Q6Layout) and a
+// bf16 activation operand in ws.
 q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t ws_bytes, int64_t m, void* y,
-                    int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream) {
+                    int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream, bool q6 = false) {
     q4k_status st = check_gemm_shape(n, k, m);
     if (st != Q4K_OK) return st;
     if (!h_ws && (st = check_output(y, m, n, out, ldy)) != Q4K_OK) return st;
@@ -151,19 +152,35 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     if ((st = device_info(&dev)) != Q4K_OK) return st;
 
     const PackedLayout W(n, k);
+    const Q6Layout W6(n, k);
     const uint8_t* wb = static_cast<const uint8_t*>(packed_w);
     uint8_t* ab = static_cast<uint8_t*>(ws);
     const int64_t kc = k / 32;
     CUtensorMap tm_x, tm_e, tm_d;
-    if ((st = encode_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ab + A.xq, k, m, 1)) != Q4K_OK) return st;
-    if ((st = encode_map(&tm_e, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ab + A.e, kc, m, 2)) != Q4K_OK) return st;
-    if ((st = encode_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb + W.ndm, kc, n, 2)) != Q4K_OK) return st;
+    if ((st = encode_map(&tm_x, q6 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ab + A.xq, k,
+                         m, 1)) != Q4K_OK)
+        return st;
+    if (q6) {   // no min term: the min-term maps are not used
+        tm_e = tm_x;
+        tm_d = tm_x;
+    } else {
+        if ((st = encode_map(&tm_e, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ab + A.e, kc, m, 2)) != Q4K_OK) return st;
+        if ((st = encode_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb + W.ndm, kc, n, 2)) != Q4K_OK) return st;
+    }
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    p.nib = wb + W.nib;
-    p.sc = wb + W.sc;
-    p.dsb = reinterpret_cast<const float*>(wb + W.dsb);
+    if (q6) {
+        p.nib = wb + W6.lo;
+        p.q6hi = wb + W6.hi;
+        p.sc = wb + W6.sc;
+        p.dsb = reinterpret_cast<const float*>(wb + W6.dsb);
+        p.q6 = 1;
+    } else {
+        p.nib = wb + W.nib;
+        p.sc = wb + W.sc;
+        p.dsb = reinterpret_cast<const float*>(wb + W.dsb);
+    }
     p.da = reinterpret_cast<const float*>(ab + A.da);
     p.y = y;
     p.dbg = dbg;
@@ -178,7 +195,7 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     p.m_tiles = static_cast<int>((m + kTileM - 1) / kTileM);
     p.n_tiles = static_cast<int>(n / kTileN);
     p.num_tiles = p.m_tiles * p.n_tiles;
-    p.n_zst = static_cast<int>(3 * ((kc + 63) / 64));
+    p.n_zst = q6 ? 0 : static_cast<int>(3 * ((kc + 63) / 64));
     p.n_main = static_cast<int>(k / 64);
     p.out_bf16 = out == Q4K_OUT_BF16 ? 1 : 0;
     // Tail balance: after the last full wave of tiles over the SMs, the R
@@ -361,7 +378,7 @@ q4k_status q4k_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, v
     if (workspace_bytes < q4k_act_workspace_bytes(m, k)) return Q4K_ERR_WORKSPACE;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != Q4K_OK) return st;
-    return from_cuda(launch_act_quantize(x, m, k, ldx, workspace, stream));
+    return from_cuda(launch_act_quantize(x, m, k, ldx, workspace, false, stream));
 }
 
 q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16_t* ssum, int64_t m, int64_t k,
@@ -375,7 +392,7 @@ q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16
     DeviceInfo* dev = nullptr;
     q4k_status st = device_info(&dev);
     if (st != Q4K_OK) return st;
-    return from_cuda(launch_act_from_q8(q8, da_f16, ssum, m, k, ldq, workspace, stream));
+    return from_cuda(launch_act_from_q8(q8, da_f16, ssum, m, k, ldq, workspace, false, stream));
 }
 
 q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k, void* workspace,
@@ -494,8 +511,28 @@ q4k_status q6k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
     if (act != Q4K_ACT_F32 && act != Q4K_ACT_Q8) return Q4K_ERR_INVALID_ARG;
     if (!aligned(packed_w, 256)) return Q4K_ERR_ALIGNMENT;
     if (m == 0) return Q4K_OK;
-    if (m > Q4K_SMALL_M || !gemv_q6k_fits(static_cast<int>(m), k)) return Q4K_ERR_SHAPE;   // decode sizes only
     DeviceInfo* dev = nullptr;
+    if (m > Q4K_SMALL_M || !gemv_q6k_fits(static_cast<int>(m), k)) {   // the tensor-core GEMM
+        if (!workspace) return Q4K_ERR_INVALID_ARG;
+        if (!aligned(workspace, 256)) return Q4K_ERR_ALIGNMENT;
+        if (workspace_bytes < q4k_act_workspace_bytes(m, k)) return Q4K_ERR_WORKSPACE;
+        if ((st = device_info(&dev)) != Q4K_OK) return st;
+        if (act == Q4K_ACT_F32) {
+            const float* xf = static_cast<const float*>(x_or_q8);
+            if ((st = check_act_f32(xf, m, k, ldx)) != Q4K_OK) return st;
+            st = from_cuda(launch_act_quantize(xf, m, k, ldx, workspace, true, stream));
+        } else {
+            const int8_t* q8 = static_cast<const int8_t*>(x_or_q8);
+            if (!q8 || !da_f16 || !ssum) return Q4K_ERR_INVALID_ARG;
+            if (ldx < k) return Q4K_ERR_SHAPE;
+            if (!aligned(q8, 4) || ldx % 4 || !aligned(da_f16, 2) || !aligned(ssum, 2)) return Q4K_ERR_ALIGNMENT;
+            st = from_cuda(launch_act_from_q8(q8, static_cast<const uint16_t*>(da_f16),
+                                              static_cast<const int16_t*>(ssum), m, k, ldx, workspace, true, stream));
+        }
+        if (st != Q4K_OK) return st;
+        return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream,
+                        true);
+    }
     if ((st = device_info(&dev)) != Q4K_OK) return st;
     const Q6Layout W(n, k);
     const uint8_t* wb = static_cast<const uint8_t*>(packed_w);
@@ -587,6 +624,15 @@ q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, 
     if (!chunk_acc) return Q4K_ERR_INVALID_ARG;
     if (m < 0 || n <= 0 || k <= 0 || m * n * (k / 32) > (int64_t(1) << 26)) return Q4K_ERR_SHAPE;
     return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, Q4K_OUT_F32, ldy, chunk_acc, nullptr, stream);
+}
+
+q4k_status q6k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, void* workspace,
+                                    size_t workspace_bytes, int64_t m, float* y, int64_t ldy, float* chunk_acc,
+                                    cudaStream_t stream) {
+    if (!chunk_acc) return Q4K_ERR_INVALID_ARG;
+    if (m < 0 || n <= 0 || k <= 0 || m * n * (k / 32) > (int64_t(1) << 26)) return Q4K_ERR_SHAPE;
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, Q4K_OUT_F32, ldy, chunk_acc, nullptr, stream,
+                    true);
 }
 
 }  // extern "C"

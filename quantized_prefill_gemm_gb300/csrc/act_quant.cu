@@ -165,14 +165,26 @@ __global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_kernel(const float* 
     ssum[t * kc + c] = static_cast<int16_t>(b.ssum);
 }
 
+// Two q8 codes as an exact 16-bit pair: fp16 (the Q4_K GEMM's operand) or
+// bf16 (the Q6_K GEMM's: its weight planes are bf16, and an MMA takes one type).
+template <bool kBf16>
+__device__ __forceinline__ uint32_t code_pair(int q0, int q1) {
+    if constexpr (kBf16) {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(static_cast<float>(q0), static_cast<float>(q1));
+        return *reinterpret_cast<const uint32_t*>(&pr);
+    } else {
+        const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+        return *reinterpret_cast<const uint32_t*>(&pr);
+    }
+}
+
+template <bool kBf16>
 __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64_t m, int64_t k, int64_t kc,
-                                              const int (&q)[4], __half da, int ssum, __half* __restrict__ xq,
+                                              const int (&q)[4], __half da, int ssum, uint16_t* __restrict__ xq,
                                               float* __restrict__ dat, __nv_bfloat16* __restrict__ e) {
-    const __half2 h01 = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
-    const __half2 h23 = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
     uint2 w;
-    w.x = *reinterpret_cast<const uint32_t*>(&h01);
-    w.y = *reinterpret_cast<const uint32_t*>(&h23);
+    w.x = code_pair<kBf16>(q[0], q[1]);
+    w.y = code_pair<kBf16>(q[2], q[3]);
     *reinterpret_cast<uint2*>(xq + t * k + c * 32 + 4 * j) = w;
     if (j == 0) {
         dat[((t >> 7) * kc + c) * 128 + (t & 127)] = __half2float(da);
@@ -183,13 +195,14 @@ __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64
     }
 }
 
-// GEMM operand form (see q4k_layout.h) from fp32 activations.  One thread
+// GEMM operand form (see q4k_layout.h; codes as fp16, or bf16 with kBf16) from fp32 activations.  One thread
 // per 32-k block: its eight 16-B loads are in flight together, amax and ssum
 // need no shuffles, and a warp covers 32 consecutive blocks of one token
 // (4 KB of contiguous fp32 in, 2 KB of fp16 and 64 + 64 B of d_a*ssum out).
+template <bool kBf16>
 __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float* __restrict__ x, int64_t m,
                                                                      int64_t mp, int64_t k, int64_t ldx,
-                                                                     __half* __restrict__ xq,
+                                                                     uint16_t* __restrict__ xq,
                                                                      float* __restrict__ dat,
                                                                      __nv_bfloat16* __restrict__ e) {
     griddep_launch_dependents();   // programmatic dependent launch (see q8_rows_kernel)
@@ -207,10 +220,7 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float
     const BlockQ8 b = quantize_block(x + t * ldx + c * 32);
     uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const __half2 pr = __halves2half2(__int2half_rn(b.q[2 * i]), __int2half_rn(b.q[2 * i + 1]));
-        w[i] = *reinterpret_cast<const uint32_t*>(&pr);
-    }
+    for (int i = 0; i < 16; ++i) w[i] = code_pair<kBf16>(b.q[2 * i], b.q[2 * i + 1]);
     uint4* dst = reinterpret_cast<uint4*>(xq + t * k + c * 32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -222,11 +232,12 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float
 }
 
 // GEMM operand form from the public q8 SoA ([m][ldq] int8, da, ssum [m][kc]).
+template <bool kBf16>
 __global__ void __launch_bounds__(kThreadsPerBlock) act_from_q8_kernel(const int8_t* __restrict__ q8,
                                                                        const uint16_t* __restrict__ da,
                                                                        const int16_t* __restrict__ ssum, int64_t m,
                                                                        int64_t mp, int64_t k, int64_t ldq,
-                                                                       __half* __restrict__ xq,
+                                                                       uint16_t* __restrict__ xq,
                                                                        float* __restrict__ dat,
                                                                        __nv_bfloat16* __restrict__ e) {
     griddep_launch_dependents();   // programmatic dependent launch (see q8_rows_kernel)
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_from_q8_kernel(const int
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = static_cast<int>(static_cast<int8_t>((w >> (8 * i)) & 0xFFu));
     const __half dh = __ushort_as_half(da[t * kc + c]);
-    write_operand(t, c, j, m, k, kc, q, dh, static_cast<int>(ssum[t * kc + c]), xq, dat, e);
+    write_operand<kBf16>(t, c, j, m, k, kc, q, dh, static_cast<int>(ssum[t * kc + c]), xq, dat, e);
 }
 
 inline unsigned grid_for(int64_t threads) {
@@ -268,27 +279,36 @@ cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_
                       ssum);
 }
 
-cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s) {
+cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, bool bf16,
+                                cudaStream_t s) {
     const ActLayout L(m, k);
     const int64_t mp = align_up(m, kTileM);
     const int64_t threads = mp * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
     if (threads == 0) return cudaSuccess;
     uint8_t* b = static_cast<uint8_t*>(ws);
-    return launch_pdl(act_quant_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp, k, ldx,
-                      reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
-                      reinterpret_cast<__nv_bfloat16*>(b + L.e));
+    uint16_t* xq = reinterpret_cast<uint16_t*>(b + L.xq);
+    float* dat = reinterpret_cast<float*>(b + L.da);
+    __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(b + L.e);
+    return bf16 ? launch_pdl(act_quant_kernel<true>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp,
+                             k, ldx, xq, dat, e)
+                : launch_pdl(act_quant_kernel<false>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp,
+                             k, ldx, xq, dat, e);
 }
 
 cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
-                               int64_t ldq, void* ws, cudaStream_t s) {
+                               int64_t ldq, void* ws, bool bf16, cudaStream_t s) {
     const ActLayout L(m, k);
     const int64_t mp = align_up(m, kTileM);
     const int64_t threads = mp * (k / 32) * 8;
     if (threads == 0) return cudaSuccess;
     uint8_t* b = static_cast<uint8_t*>(ws);
-    return launch_pdl(act_from_q8_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da, ssum, m, mp,
-                      k, ldq, reinterpret_cast<__half*>(b + L.xq), reinterpret_cast<float*>(b + L.da),
-                      reinterpret_cast<__nv_bfloat16*>(b + L.e));
+    uint16_t* xq = reinterpret_cast<uint16_t*>(b + L.xq);
+    float* dat = reinterpret_cast<float*>(b + L.da);
+    __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(b + L.e);
+    return bf16 ? launch_pdl(act_from_q8_kernel<true>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da,
+                             ssum, m, mp, k, ldq, xq, dat, e)
+                : launch_pdl(act_from_q8_kernel<false>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da,
+                             ssum, m, mp, k, ldq, xq, dat, e);
 }
 
 }  // namespace q4k

@@ -40,40 +40,49 @@
 #include "q4k_internal.h"
 #include "q4k_layout.h"
 #include "q4k_ptx.cuh"
+#include "q4k_unpack.cuh"
 
 namespace q4k {
 namespace {
 
-constexpr int kStages = 5;
 constexpr int kThreads = 448;
-constexpr uint32_t kStageA = 16384;   // 128 rows x 64 fp16 / bf16
-constexpr uint32_t kStageB = 16384;
-constexpr uint32_t kStageNib = 4096;  // 2 chunks x 128 rows x 16 B
-constexpr uint32_t kStageSc = 256;    // 2 chunks x 128 rows
-constexpr uint32_t kStageDa = 1024;   // 2 chunks x 128 tokens x fp32
-constexpr uint32_t kStageD = 512;     // 128 rows x fp32 (last stage of a super-block)
 
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kStageA;
-constexpr uint32_t kOffNib = kOffB + kStages * kStageB;
-constexpr uint32_t kOffSc = kOffNib + kStages * kStageNib;
-constexpr uint32_t kOffDa = kOffSc + kStages * kStageSc;
-constexpr uint32_t kOffD = kOffDa + kStages * kStageDa;
-constexpr uint32_t kOffBar = kOffD + kStages * kStageD;
-// barrier indices
-constexpr int kBarFull = 0;                 // [kStages] producer -> all (tx bytes)
-constexpr int kBarConv = kStages;           // [kStages] converters -> MMA (4 arrivals, every stage)
-constexpr int kBarEmpty = 2 * kStages;      // [kStages] MMA commit + 8 epilogue warps -> producer
-constexpr int kBarAccFull = 3 * kStages;    // [2] MMA commit -> epilogue
-constexpr int kBarAccEmpty = kBarAccFull + 2;   // [2] 8 epilogue warps -> MMA
-constexpr int kBarZ = kBarAccEmpty + 2;     // [2] MMA commit (min term done) -> epilogue
-constexpr int kBarYEmpty = kBarZ + 2;       // [2] 8 epilogue warps -> MMA
-constexpr int kBarDrain = kBarYEmpty + 2;   // MMA's final commit
-constexpr int kNumBars = kBarDrain + 1;
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
-constexpr size_t kSmemBytes = kSmemUsed + 1024;         // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// Shared-memory carve-out per format.  Q4_K: five stages of the fp16 A tile,
+// the fp16 B tile (sc*q), the packed quants, sc, d_a and d.  Q6_K: four stages
+// (the B tile has two bf16 planes, hi and lo) plus the high quant bits.
+template <bool kQ6>
+struct Lay {
+    static constexpr int kStages = kQ6 ? 4 : 5;
+    static constexpr uint32_t kStageA = 16384;                  // 128 rows x 64 fp16 / bf16
+    static constexpr uint32_t kStageB = kQ6 ? 32768 : 16384;    // Q6_K: hi plane, then lo plane
+    static constexpr uint32_t kStageNib = 4096;                 // 2 chunks x 128 rows x 16 B
+    static constexpr uint32_t kStageHi = kQ6 ? 2048 : 0;        // 2 chunks x 128 rows x 8 B
+    static constexpr uint32_t kStageSc = kQ6 ? 512 : 256;       // 2 chunks x 128 rows x (2 or 1) B
+    static constexpr uint32_t kStageDa = 1024;                  // 2 chunks x 128 tokens x fp32
+    static constexpr uint32_t kStageD = 512;                    // 128 rows x fp32 (last stage of a super-block)
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kOffA + kStages * kStageA;
+    static constexpr uint32_t kOffNib = kOffB + kStages * kStageB;
+    static constexpr uint32_t kOffHi = kOffNib + kStages * kStageNib;
+    static constexpr uint32_t kOffSc = kOffHi + kStages * kStageHi;
+    static constexpr uint32_t kOffDa = kOffSc + kStages * kStageSc;
+    static constexpr uint32_t kOffD = kOffDa + kStages * kStageDa;
+    static constexpr uint32_t kOffBar = kOffD + kStages * kStageD;
+    // barrier indices
+    static constexpr int kBarFull = 0;                       // [kStages] producer -> all (tx bytes)
+    static constexpr int kBarConv = kStages;                 // [kStages] converters -> MMA (4 arrivals)
+    static constexpr int kBarEmpty = 2 * kStages;            // [kStages] MMA commit + 8 epilogue warps -> producer
+    static constexpr int kBarAccFull = 3 * kStages;          // [2] MMA commit -> epilogue
+    static constexpr int kBarAccEmpty = kBarAccFull + 2;     // [2] 8 epilogue warps -> MMA
+    static constexpr int kBarZ = kBarAccEmpty + 2;           // [2] MMA commit (min term done) -> epilogue
+    static constexpr int kBarYEmpty = kBarZ + 2;             // [2] 8 epilogue warps -> MMA
+    static constexpr int kBarDrain = kBarYEmpty + 2;         // MMA's final commit
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag
+    static constexpr uint32_t kSmemUsed = kOffMisc + 16;
+    static constexpr size_t kSmemBytes = kSmemUsed + 1024;          // + alignment slack
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 constexpr uint32_t kIdescMain = idesc_kind_f16(128, 128, false);   // fp16 x fp16 -> fp32
 constexpr uint32_t kIdescMin = idesc_kind_f16(128, 128, true);     // bf16 x bf16 -> fp32
@@ -84,14 +93,16 @@ enum : unsigned {
     kSiteConvFull, kSiteEpiFull, kSiteEpiAccFull, kSiteEpiZ
 };
 
+template <bool kQ6>
 struct Ctx {
+    using L = Lay<kQ6>;
     uint32_t base;      // shared address of the 1024-aligned carve-out
     uint8_t* sbase;     // generic pointer to the same
     uint32_t tmem;      // TMEM base address (lane 0, column 0)
     volatile int* abort_flag;
-    __device__ uint32_t bar(int i) const { return base + kOffBar + 8u * static_cast<uint32_t>(i); }
-    __device__ uint32_t a(int s) const { return base + kOffA + kStageA * s; }
-    __device__ uint32_t b(int s) const { return base + kOffB + kStageB * s; }
+    __device__ uint32_t bar(int i) const { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); }
+    __device__ uint32_t a(int s) const { return base + L::kOffA + L::kStageA * s; }
+    __device__ uint32_t b(int s) const { return base + L::kOffB + L::kStageB * s; }
     __device__ bool wait(const GemmParams& p, int barrier, uint32_t parity, unsigned site) const {
         return mbar_wait(bar(barrier), parity, abort_flag, p.timeout_cycles, p.err, site);
     }
@@ -102,8 +113,9 @@ struct Ctx {
     }
 };
 
+template <bool kQ6>
 __device__ __forceinline__ void advance(int& s, uint32_t& ph) {
-    if (++s == kStages) {
+    if (++s == Lay<kQ6>::kStages) {
         s = 0;
         ph ^= 1u;
     }
@@ -144,8 +156,10 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
 }
 
 // ------------------------------------------------------------- producer --
-__device__ __forceinline__ void run_producer(const Ctx& cx, const GemmParams& p, const CUtensorMap* tm_x,
+template <bool kQ6>
+__device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParams& p, const CUtensorMap* tm_x,
                                              const CUtensorMap* tm_e, const CUtensorMap* tm_d) {
+    using L = Lay<kQ6>;
     int s = 0;
     uint32_t ph = 0, issued = 0, parity_bits = 0;
     bool ok = true;
@@ -153,43 +167,51 @@ __device__ __forceinline__ void run_producer(const Ctx& cx, const GemmParams& p,
         const Unit w = unit_of(p, u);
         const int mt = w.mt, nt = w.nt;
         for (int st = 0; st < w.n_st; ++st) {
-            if (!cx.wait(p, kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
+            if (!cx.wait(p, L::kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
                 ok = false;
                 break;
             }
-            const uint32_t fb = cx.bar(kBarFull + s);
+            const uint32_t fb = cx.bar(L::kBarFull + s);
             if (st + w.kbase < 0) {
                 const int j = st / 3, part = st - 3 * j;   // part 0: hi*hi, 1: hi*lo, 2: lo*hi
-                mbar_arrive_expect_tx(fb, kStageA + kStageB);
+                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageB);
                 tma_load_3d(cx.a(s), tm_e, fb, 64 * j, 128 * mt, part == 2 ? 1 : 0);
                 tma_load_3d(cx.b(s), tm_d, fb, 64 * j, 128 * nt, part == 1 ? 1 : 0);
             } else {
                 const int kb = st + w.kbase;
                 const bool sb_last = (kb & 3) == 3;
-                mbar_arrive_expect_tx(fb, kStageA + kStageNib + kStageSc + kStageDa + (sb_last ? kStageD : 0u));
+                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageNib + L::kStageHi + L::kStageSc + L::kStageDa +
+                                              (sb_last ? L::kStageD : 0u));
                 tma_load_2d(cx.a(s), tm_x, fb, 64 * kb, 128 * mt);
                 const int64_t rec = static_cast<int64_t>(nt) * p.kc + 2 * kb;
-                bulk_load(cx.base + kOffNib + kStageNib * s, p.nib + rec * 128 * 16, kStageNib, fb);
-                bulk_load(cx.base + kOffSc + kStageSc * s, p.sc + rec * 128, kStageSc, fb);
-                bulk_load(cx.base + kOffDa + kStageDa * s, p.da + (static_cast<int64_t>(mt) * p.kc + 2 * kb) * 128,
-                          kStageDa, fb);
+                bulk_load(cx.base + L::kOffNib + L::kStageNib * s, p.nib + rec * 128 * 16, L::kStageNib, fb);
+                if constexpr (kQ6) {   // high quant bits, and two scales per row and chunk
+                    bulk_load(cx.base + L::kOffHi + L::kStageHi * s, p.q6hi + rec * 128 * 8, L::kStageHi, fb);
+                    bulk_load(cx.base + L::kOffSc + L::kStageSc * s, p.sc + rec * 128 * 2, L::kStageSc, fb);
+                } else {
+                    bulk_load(cx.base + L::kOffSc + L::kStageSc * s, p.sc + rec * 128, L::kStageSc, fb);
+                }
+                bulk_load(cx.base + L::kOffDa + L::kStageDa * s, p.da + (static_cast<int64_t>(mt) * p.kc + 2 * kb) * 128,
+                          L::kStageDa, fb);
                 if (sb_last)
-                    bulk_load(cx.base + kOffD + kStageD * s,
-                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + (kb >> 2)) * 128, kStageD, fb);
+                    bulk_load(cx.base + L::kOffD + L::kStageD * s,
+                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + (kb >> 2)) * 128, L::kStageD, fb);
             }
             issued |= 1u << s;
             parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
-            advance(s, ph);
+            advance<kQ6>(s, ph);
         }
     }
     if (!ok) {   // let every copy this thread started land before the CTA exits
-        for (int i = 0; i < kStages; ++i)
-            if ((issued >> i) & 1u) mbar_wait_quiet(cx.bar(kBarFull + i), (parity_bits >> i) & 1u, p.timeout_cycles);
+        for (int i = 0; i < L::kStages; ++i)
+            if ((issued >> i) & 1u) mbar_wait_quiet(cx.bar(L::kBarFull + i), (parity_bits >> i) & 1u, p.timeout_cycles);
     }
 }
 
 // ----------------------------------------------------------- MMA issuer --
-__device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
+template <bool kQ6>
+__device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p) {
+    using L = Lay<kQ6>;
     int s = 0, ab = 0, it = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
@@ -197,14 +219,14 @@ __device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
         const Unit w = unit_of(p, u);
         const int yb = it & 1;
         const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
-        if (!cx.wait(p, kBarYEmpty + yb, yph ^ 1u, kSiteMmaYEmpty)) break;
+        if (!cx.wait(p, L::kBarYEmpty + yb, yph ^ 1u, kSiteMmaYEmpty)) break;
         tc_fence_after();
         const uint32_t ty = cx.tmem + 256u + 128u * yb;
         // a unit without min-term stages still completes the buffer's Z phase
         // (nothing to wait for: the epilogue starts Y at zero itself)
-        if (w.kbase >= 0) tc_commit(cx.bar(kBarZ + yb));
+        if (w.kbase >= 0) tc_commit(cx.bar(L::kBarZ + yb));
         for (int st = 0; st < w.n_st; ++st) {
-            if (!cx.wait(p, kBarFull + s, ph, kSiteMmaFull)) {
+            if (!cx.wait(p, L::kBarFull + s, ph, kSiteMmaFull)) {
                 ok = false;
                 break;
             }
@@ -215,49 +237,106 @@ __device__ __forceinline__ void run_mma(const Ctx& cx, const GemmParams& p) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
                     tc_mma_f16(ty, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
-                tc_commit(cx.bar(kBarEmpty + s));
-                if (st + w.kbase == -1) tc_commit(cx.bar(kBarZ + yb));
+                tc_commit(cx.bar(L::kBarEmpty + s));
+                if (st + w.kbase == -1) tc_commit(cx.bar(L::kBarZ + yb));
             } else {
-                if (!cx.wait(p, kBarConv + s, ph, kSiteMmaConv)) {
+                if (!cx.wait(p, L::kBarConv + s, ph, kSiteMmaConv)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // the two 32-k chunks of this stage
-                    if (!cx.wait(p, kBarAccEmpty + ab, aph ^ 1u, kSiteMmaAccEmpty)) {
+                    if (!cx.wait(p, L::kBarAccEmpty + ab, aph ^ 1u, kSiteMmaAccEmpty)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t tj = cx.tmem + 128u * ab;
-                    tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
-                    tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
-                    tc_commit(cx.bar(kBarAccFull + ab));
+                    if constexpr (kQ6) {   // bf16: the hi plane, then the lo plane, into one accumulator
+                        const uint64_t bl = sw128_kmajor_desc(cx.b(s) + L::kStageB / 2);
+                        tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMin, 0u);
+                        tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMin, 1u);
+                        tc_mma_f16(tj, ad + 4u * h, bl + 4u * h, kIdescMin, 1u);
+                        tc_mma_f16(tj, ad + 4u * h + 2u, bl + 4u * h + 2u, kIdescMin, 1u);
+                    } else {
+                        tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
+                        tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
+                    }
+                    tc_commit(cx.bar(L::kBarAccFull + ab));
                     if (++ab == 2) {
                         ab = 0;
                         aph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(cx.bar(kBarEmpty + s));
+                tc_commit(cx.bar(L::kBarEmpty + s));
             }
-            advance(s, ph);
+            advance<kQ6>(s, ph);
         }
     }
     // every MMA this thread issued has finished before the CTA tears down
-    tc_commit(cx.bar(kBarDrain));
-    mbar_wait_quiet(cx.bar(kBarDrain), 0u, p.timeout_cycles);
+    tc_commit(cx.bar(L::kBarDrain));
+    mbar_wait_quiet(cx.bar(L::kBarDrain), 0u, p.timeout_cycles);
 }
 
 // ------------------------------------------------------------ converters --
+// Q6_K: row r of stage s.  Each weight's exact integer a = sc * (q - 32)
+// (|a| <= 4096, exact in fp32) becomes hi = bf16(a) and lo = a - hi (exact
+// in bf16); the two bf16 planes go to the two halves of the B tile, so that
+// two MMAs per 16 k add hi*qa + lo*qa = a*qa into the accumulator.  With
+// max |hi| + |lo| = 4096 over all (sc, q), every partial sum of a 32-k
+// chunk stays below 32 * 4096 * 127 < 2^24: the chunk integer is exact.
+template <bool kQ6>
+__device__ __forceinline__ void convert_q6(const Ctx<kQ6>& cx, int s, int r, uint32_t rx, uint32_t row_off) {
+    using L = Lay<kQ6>;
+    const uint8_t* lo = cx.sbase + L::kOffNib + L::kStageNib * s;
+    const uint8_t* hi = cx.sbase + L::kOffHi + L::kStageHi * s;
+    const uint8_t* scs = cx.sbase + L::kOffSc + L::kStageSc * s;
+    uint8_t* bhi = cx.sbase + L::kOffB + L::kStageB * s + row_off;
+    uint8_t* blo = bhi + L::kStageB / 2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint4 wl = *reinterpret_cast<const uint4*>(lo + (h * 128 + r) * 16);
+        const uint2 wh = *reinterpret_cast<const uint2*>(hi + (h * 128 + r) * 8);
+        const uint32_t scp = *reinterpret_cast<const uint16_t*>(scs + (h * 128 + r) * 2);
+        const float sc0 = static_cast<float>(static_cast<int8_t>(scp & 0xFFu));
+        const float sc1 = static_cast<float>(static_cast<int8_t>(scp >> 8));
+        const uint32_t lw[4] = {wl.x, wl.y, wl.z, wl.w};
+        const uint32_t hw[4] = {wh.x, wh.x >> 2, wh.y, wh.y >> 2};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // 8-k group i of chunk h
+            uint32_t v[2];
+            unpack_q6(lw[i], hw[i], v[0], v[1]);
+            const float sc = i < 2 ? sc0 : sc1;
+            uint32_t ohi[4], olo[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t w = v[jj >> 1] >> (16 * (jj & 1));
+                const float a0 = static_cast<float>(static_cast<int8_t>(w & 0xFFu)) * sc;
+                const float a1 = static_cast<float>(static_cast<int8_t>((w >> 8) & 0xFFu)) * sc;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+                const float2 hf = __bfloat1622float2(h2);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(__fsub_rn(a0, hf.x), __fsub_rn(a1, hf.y));
+                ohi[jj] = *reinterpret_cast<const uint32_t*>(&h2);
+                olo[jj] = *reinterpret_cast<const uint32_t*>(&l2);
+            }
+            const uint32_t g = static_cast<uint32_t>(4 * h + i);
+            *reinterpret_cast<uint4*>(bhi + ((g ^ rx) << 4)) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+            *reinterpret_cast<uint4*>(blo + ((g ^ rx) << 4)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+        }
+    }
+}
+
 // Each thread owns one od row r of the tile.  For chunk h of the stage it
 // reads the row's 16 B of quants (4 words, one per 8-k group) and its sc,
 // and writes four 16-B granules of fp16 sc*q into row r of the B tile at the
 // 128-B-swizzled positions (granule g of row r lands at g ^ (r & 7)).  A
 // group of 8 consecutive lanes covers 8 consecutive rows: the 16-B reads are
 // contiguous and the granule writes fall in 8 distinct bank quads.
-__device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p, int ci, int lane) {
+template <bool kQ6>
+__device__ __forceinline__ void run_converter(const Ctx<kQ6>& cx, const GemmParams& p, int ci, int lane) {
+    using L = Lay<kQ6>;
     const int r = ci * 32 + lane;
     const uint32_t rx = static_cast<uint32_t>(r & 7);
     const uint32_t row_off = static_cast<uint32_t>(r >> 3) * 1024u + rx * 128u;
@@ -268,7 +347,7 @@ __device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
         for (int st = 0; st < w.n_st; ++st) {
-            if (!cx.warp_wait(p, kBarFull + s, ph, kSiteConvFull)) {
+            if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteConvFull)) {
                 ok = false;
                 break;
             }
@@ -277,11 +356,16 @@ __device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p
                 // every stage barrier completes exactly one phase per ring pass
                 // and the MMA's phase bit stays valid for it
                 __syncwarp();
-                if (lane == 0) mbar_arrive(cx.bar(kBarConv + s));
+                if (lane == 0) mbar_arrive(cx.bar(L::kBarConv + s));
+            } else if constexpr (kQ6) {
+                convert_q6(cx, s, r, rx, row_off);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cx.bar(L::kBarConv + s));
             } else {
-                const uint8_t* nib = cx.sbase + kOffNib + kStageNib * s;
-                const uint8_t* scs = cx.sbase + kOffSc + kStageSc * s;
-                uint8_t* brow = cx.sbase + kOffB + kStageB * s + row_off;
+                const uint8_t* nib = cx.sbase + L::kOffNib + L::kStageNib * s;
+                const uint8_t* scs = cx.sbase + L::kOffSc + L::kStageSc * s;
+                uint8_t* brow = cx.sbase + L::kOffB + L::kStageB * s + row_off;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint4 w = *reinterpret_cast<const uint4*>(nib + (h * 128 + r) * 16);
@@ -305,9 +389,9 @@ __device__ __forceinline__ void run_converter(const Ctx& cx, const GemmParams& p
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(cx.bar(kBarConv + s));
+                if (lane == 0) mbar_arrive(cx.bar(L::kBarConv + s));
             }
-            advance(s, ph);
+            advance<kQ6>(s, ph);
         }
     }
 }
@@ -452,8 +536,9 @@ __device__ __noinline__ void store_partial(const GemmParams& p, uint32_t ty, int
     }
 }
 
-template <bool kDump, bool kSwiGLU>
-__device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p, int warp, int e, int lane) {
+template <bool kDump, bool kSwiGLU, bool kQ6>
+__device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParams& p, int warp, int e, int lane) {
+    using L = Lay<kQ6>;
     const int qd = warp & 3, ch = e >> 2;
     const int row = qd * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
@@ -481,17 +566,17 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
             tmem_wait_st();
         }
         for (int st = 0; ok && st < w.n_st; ++st) {
-            if (!cx.warp_wait(p, kBarFull + s, ph, kSiteEpiFull)) {
+            if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteEpiFull)) {
                 ok = false;
                 break;
             }
             const int kb = st + w.kbase;
             if (kb >= 0) {
-                const float* das = reinterpret_cast<const float*>(cx.sbase + kOffDa + kStageDa * s);
+                const float* das = reinterpret_cast<const float*>(cx.sbase + L::kOffDa + L::kStageDa * s);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float da = das[h * 128 + row];
-                    if (ok && !cx.warp_wait(p, kBarAccFull + ab, aph, kSiteEpiAccFull)) ok = false;
+                    if (ok && !cx.warp_wait(p, L::kBarAccFull + ab, aph, kSiteEpiAccFull)) ok = false;
                     if (ok) {
                         tc_fence_after();
                         const uint32_t tj = cx.tmem + lane_off + 128u * ab + 64u * ch;
@@ -503,7 +588,7 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
                             if (q == 3) {   // whole buffer read: hand it back to the MMA
                                 tc_fence_before();
                                 __syncwarp();
-                                if (lane == 0) mbar_arrive(cx.bar(kBarAccEmpty + ab));
+                                if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + ab));
                             }
 #pragma unroll
                             for (int j = 0; j < 16; j += 2)
@@ -520,14 +605,14 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
                 if (!ok) break;
                 if ((kb & 3) == 3) {   // super-block done: Y += d * P
                     if (!zready) {
-                        if (!cx.warp_wait(p, kBarZ + yb, yph, kSiteEpiZ)) {
+                        if (!cx.warp_wait(p, L::kBarZ + yb, yph, kSiteEpiZ)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         zready = true;
                     }
-                    const float* dv = reinterpret_cast<const float*>(cx.sbase + kOffD + kStageD * s) + 64 * ch;
+                    const float* dv = reinterpret_cast<const float*>(cx.sbase + L::kOffD + L::kStageD * s) + 64 * ch;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t Yv[16];
@@ -549,15 +634,15 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(kBarEmpty + s));
-            advance(s, ph);
+            if (lane == 0) mbar_arrive(cx.bar(L::kBarEmpty + s));
+            advance<kQ6>(s, ph);
         }
         if (!ok) break;
         if (w.slot >= 0) {   // a k-part of a split tile: its partial Y, finished by the fixup kernel
             store_partial(p, ty, w.slot, qd * 2 + ch, lane);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
+            if (lane == 0) mbar_arrive(cx.bar(L::kBarYEmpty + yb));
         } else if constexpr (kSwiGLU) {
             // tile done: the 64 columns are 32 gate and 32 up outputs of the
             // down projection's input chunk c = 2 nt + ch
@@ -569,7 +654,7 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
+            if (lane == 0) mbar_arrive(cx.bar(L::kBarYEmpty + yb));
             const int c = 2 * nt + ch;
             if (t < p.m)
                 swiglu_store(p, t, c, g0, g1, u0, u1);
@@ -586,7 +671,7 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(kBarYEmpty + yb));
+            if (lane == 0) mbar_arrive(cx.bar(L::kBarYEmpty + yb));
         }
     }
 }
@@ -594,37 +679,39 @@ __device__ __forceinline__ void run_epilogue(const Ctx& cx, const GemmParams& p,
 // kDump: also write every per-chunk accumulator to p.dbg (test hook build).
 // kSwiGLU: gate/up pair weights; the tile end writes the down projection's
 // q8 operand of SiLU(gate)*up instead of Y.
-template <bool kDump, bool kSwiGLU>
+// kQ6: Q6_K weights (Q6Layout) and a bf16 activation operand.
+template <bool kDump, bool kSwiGLU, bool kQ6>
 __global__ void __launch_bounds__(kThreads, 1)
     q4k_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_e,
                     const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
+    using L = Lay<kQ6>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    Ctx cx;
+    Ctx<kQ6> cx;
     cx.base = base;
     cx.sbase = smem_raw + (base - raw);
-    cx.abort_flag = reinterpret_cast<volatile int*>(cx.sbase + kOffMisc + 4);
+    cx.abort_flag = reinterpret_cast<volatile int*>(cx.sbase + L::kOffMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(cx.bar(kBarFull + s), 1);
-            mbar_init(cx.bar(kBarConv + s), 4);
-            mbar_init(cx.bar(kBarEmpty + s), 9);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(cx.bar(L::kBarFull + s), 1);
+            mbar_init(cx.bar(L::kBarConv + s), 4);
+            mbar_init(cx.bar(L::kBarEmpty + s), 9);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(cx.bar(kBarAccFull + b), 1);
-            mbar_init(cx.bar(kBarAccEmpty + b), 8);
-            mbar_init(cx.bar(kBarZ + b), 1);
-            mbar_init(cx.bar(kBarYEmpty + b), 8);
+            mbar_init(cx.bar(L::kBarAccFull + b), 1);
+            mbar_init(cx.bar(L::kBarAccEmpty + b), 8);
+            mbar_init(cx.bar(L::kBarZ + b), 1);
+            mbar_init(cx.bar(L::kBarYEmpty + b), 8);
         }
-        mbar_init(cx.bar(kBarDrain), 1);
+        mbar_init(cx.bar(L::kBarDrain), 1);
         *cx.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(base + kOffMisc, 512);
+    if (warp == 0) tmem_alloc(base + L::kOffMisc, 512);
     if (warp == 1 && lane == 0) {
         prefetch_tmap(&tm_x);
         prefetch_tmap(&tm_e);
@@ -633,22 +720,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.sbase + kOffMisc);
+    cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.sbase + L::kOffMisc);
     // launched with programmatic dependent launch: the set-up above overlaps
     // the previous kernel's tail; its results (the activation operand) are
     // read, and Y or the workspace written, only after it has completed
     griddep_wait();
 
     if (warp == 0) {
-        if (lane == 0) run_producer(cx, p, &tm_x, &tm_e, &tm_d);
+        if (lane == 0) run_producer<kQ6>(cx, p, &tm_x, &tm_e, &tm_d);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) run_mma(cx, p);
+        if (lane == 0) run_mma<kQ6>(cx, p);
         __syncwarp();
     } else if (warp < 6) {
-        run_converter(cx, p, warp - 2, lane);
+        run_converter<kQ6>(cx, p, warp - 2, lane);
     } else {
-        run_epilogue<kDump, kSwiGLU>(cx, p, warp, warp - 6, lane);
+        run_epilogue<kDump, kSwiGLU, kQ6>(cx, p, warp, warp - 6, lane);
     }
 
     tc_fence_before();
@@ -776,26 +863,35 @@ __global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_cycles) {
     __syncthreads();
 }
 
-}  // namespace
-
-cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
-                        const GemmParams& p, int grid, cudaStream_t s) {
-    static bool attr_set[64][3] = {};
+template <bool kDump, bool kSwiGLU, bool kQ6>
+cudaError_t launch_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
+                           const GemmParams& p, int grid, cudaStream_t s) {
+    static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (p.dbg && p.hq) return cudaErrorInvalidValue;
-    const int variant = p.dbg ? 1 : (p.hq ? 2 : 0);
-    void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const GemmParams) =
-        variant == 1 ? q4k_gemm_kernel<true, false> : (variant == 2 ? q4k_gemm_kernel<false, true>
-                                                                     : q4k_gemm_kernel<false, false>);
-    if (!attr_set[dev][variant]) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    constexpr size_t smem = Lay<kQ6>::kSmemBytes;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(q4k_gemm_kernel<kDump, kSwiGLU, kQ6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_set[dev][variant] = true;
+        attr_set[dev] = true;
     }
-    return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, tm_x, tm_e, tm_d, p);
+    return launch_pdl(q4k_gemm_kernel<kDump, kSwiGLU, kQ6>, dim3(grid), dim3(kThreads), smem, s, tm_x, tm_e, tm_d, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
+                        const GemmParams& p, int grid, cudaStream_t s) {
+    if (p.hq && (p.dbg || p.q6)) return cudaErrorInvalidValue;
+    if (p.q6)
+        return p.dbg ? launch_variant<true, false, true>(tm_x, tm_e, tm_d, p, grid, s)
+                     : launch_variant<false, false, true>(tm_x, tm_e, tm_d, p, grid, s);
+    if (p.hq) return launch_variant<false, true, false>(tm_x, tm_e, tm_d, p, grid, s);
+    return p.dbg ? launch_variant<true, false, false>(tm_x, tm_e, tm_d, p, grid, s)
+                 : launch_variant<false, false, false>(tm_x, tm_e, tm_d, p, grid, s);
 }
 
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s) {

@@ -37,6 +37,7 @@
 
 #include "q4k_internal.h"
 #include "q4k_ptx.cuh"
+#include "q4k_unpack.cuh"
 
 namespace q4k {
 namespace {
@@ -45,18 +46,6 @@ constexpr int kRows = 16;      // od rows per CTA
 constexpr int kParts = 16;     // super-block shares per row (2 per warp)
 constexpr int kThreads = 256;
 constexpr size_t kPersistMaxSmem = 220 * 1024;   // persistent form: activations + partial sums
-
-// 4-bit quants of one 8-k group (one packed word) -> two words of 4 bytes in
-// k order.  In the packed word the nibble at bits 4j is k = 2j and the nibble
-// at bits 16 + 4j is k = 2j + 1.
-__device__ __forceinline__ void unpack_group(uint32_t w, uint32_t& k0123, uint32_t& k4567) {
-    const uint32_t a = w & 0x000F000Fu;           // bytes 0, 2: k0, k1
-    const uint32_t b = (w >> 4) & 0x000F000Fu;    // bytes 0, 2: k2, k3
-    const uint32_t c = (w >> 8) & 0x000F000Fu;    // k4, k5
-    const uint32_t e = (w >> 12) & 0x000F000Fu;   // k6, k7
-    k0123 = __byte_perm(a, b, 0x6420);
-    k4567 = __byte_perm(c, e, 0x6420);
-}
 
 // Activations of one super-block for M tokens.
 template <int M>
@@ -487,16 +476,6 @@ __device__ __forceinline__ void load_weights_q6(const GemvParams& p, int64_t nt,
         w.hi[j] = __ldg(reinterpret_cast<const uint2*>(p.q6hi) + rec0 + 128 * j);
         w.sc[j] = __ldg(reinterpret_cast<const uint16_t*>(p.sc) + rec0 + 128 * j);
     }
-}
-
-// Signed bytes q - 32 of 8-k group g: lo word, and the hi word shifted to the group.
-__device__ __forceinline__ void unpack_q6(uint32_t lo, uint32_t hi, uint32_t& v0123, uint32_t& v4567) {
-    uint32_t l0, l1, h0, h1;
-    unpack_group(lo, l0, l1);
-    unpack_group(hi & 0x33333333u, h0, h1);
-    const uint32_t u0 = l0 | (h0 << 4), u1 = l1 | (h1 << 4);   // 6-bit u per byte
-    v0123 = u0 | ((u0 & 0x20202020u) * 6u);                     // copy bit 5 into bits 6 and 7
-    v4567 = u1 | ((u1 & 0x20202020u) * 6u);
 }
 
 template <int M, bool kQuant>

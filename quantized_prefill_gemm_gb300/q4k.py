@@ -55,6 +55,8 @@ SIGNATURES = {
     "q6k_pack_weights": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_ptr]),
     "q6k_gemm": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
                           _c_ptr, _c_int, _c_i64, _c_ptr, _c_size, _c_ptr]),
+    "q6k_gemm_debug_chunk_acc": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_i64,
+                                          _c_ptr, _c_ptr]),
     "q4k_static_workspace_bytes": (_c_size, []),
     "q4k_gemm_static_workspace": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64,
                                            _c_ptr, _c_int, _c_i64, _c_ptr]),
@@ -325,6 +327,17 @@ def q4k_gemm_debug_chunk_acc(packed, n, k, workspace, m, stream=None):
     y = torch.empty((m, n), dtype=torch.float32, device=packed.device)
     acc = torch.zeros((m, n, k // 32), dtype=torch.float32, device=packed.device)
     _check("q4k_gemm_debug_chunk_acc", LIB.q4k_gemm_debug_chunk_acc(
+        _dev(packed, "packed"), n, k, _dev(workspace, "workspace"), workspace.numel(), m, _dev(y, "y"), n,
+        _dev(acc, "acc"), _stream(stream)))
+    return y, acc
+
+
+def q6k_gemm_debug_chunk_acc(packed, n, k, workspace, m, stream=None):
+    """Test hook for Q6_K (workspace: the bf16 operand a q6k_gemm call with m > 16 left in it):
+    (y fp32 [m][n], J fp32 [m][n][k/32]) with J the exact per-chunk integers."""
+    y = torch.empty((m, n), dtype=torch.float32, device=packed.device)
+    acc = torch.zeros((m, n, k // 32), dtype=torch.float32, device=packed.device)
+    _check("q6k_gemm_debug_chunk_acc", LIB.q6k_gemm_debug_chunk_acc(
         _dev(packed, "packed"), n, k, _dev(workspace, "workspace"), workspace.numel(), m, _dev(y, "y"), n,
         _dev(acc, "acc"), _stream(stream)))
     return y, acc

@@ -1,4 +1,5 @@
-"""q6k_gemm (Q6_K weights, decode sizes) on the GPU vs the oracle.
+"""q6k_gemm (Q6_K weights) on the GPU vs the oracle: the small-M path for
+decode sizes and the tensor-core GEMM above them.
 
 Bar as for Q4_K: per element |y_gpu - y_oracle| <= 1e-4 * sum_k |w_k * a_k|
 (plus one bf16 rounding for bf16 output); fp32 activations quantized inside
@@ -77,12 +78,50 @@ def test_in_kernel_quantization_bits(q4k, m):
     assert torch.equal(a, b) and torch.equal(a, c)
 
 
-def test_rejects_prefill_sizes(q4k):
-    n, k = 256, 512
-    packed = q4k.q6k_pack_weights(to_dev(inputs.q6k_blocks(n, k, 1)), n, k)
-    with pytest.raises(q4k.Q4KError):
-        q4k.q6k_gemm(packed, n, k, torch.zeros((17, k), dtype=torch.float32, device=DEV))
-    big = 14336
-    packed = q4k.q6k_pack_weights(to_dev(inputs.q6k_blocks(n, big, 1)), n, big)
-    with pytest.raises(q4k.Q4KError):   # 16 x 14336 activations do not fit the kernel's shared memory
-        q4k.q6k_gemm(packed, n, big, torch.zeros((16, big), dtype=torch.float32, device=DEV))
+@pytest.mark.parametrize("m,n,k,out,act", [(17, 128, 256, "f32", "f32"), (64, 256, 512, "f32", "q8"),
+                                            (200, 384, 768, "bf16", "f32"), (300, 256, 2816, "f32", "q8")])
+def test_prefill_sizes_tensor_core_path(q4k, m, n, k, out, act):
+    """m > 16: the tcgen05 GEMM with bf16 hi/lo weight planes (every output,
+    ragged token tiles, the k-split of the last wave)."""
+    _check(q4k, n, k, m, 90 + m, out=out, act=act, kind="outlier")
+
+
+def test_prefill_chunk_integers_exact(q4k):
+    """Every per-chunk accumulator of the tensor-core path equals the oracle's
+    exact integer sum_s sc_s * sum (q - 32) * qa: the hi/lo split and the fp32
+    accumulator lose nothing."""
+    m, n, k = 64, 256, 512
+    blocks = inputs.q6k_blocks(n, k, 5)
+    x = inputs.activations(m, k, 5, "outlier")
+    packed = q4k.q6k_pack_weights(to_dev(blocks), n, k)
+    ws = torch.empty(q4k.q4k_act_workspace_bytes(m, k), dtype=torch.uint8, device=DEV)
+    y = q4k.q6k_gemm(packed, n, k, to_dev(x), workspace=ws)   # leaves the bf16 operand in ws
+    y2, acc = q4k.q6k_gemm_debug_chunk_acc(packed, n, k, ws, m)
+    torch.cuda.synchronize()
+    f = oq6.decode(blocks)
+    qa, _, _ = oq8.quantize_rows(x)
+    ints = oq6.chunk_ints(f, qa)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ints)
+    assert torch.equal(y, y2)
+
+
+def test_prefill_full_size_sampled(q4k):
+    """2048 tokens through a 4096 x 11008 Q6_K matrix (a 7B down projection):
+    sampled rows against the oracle."""
+    from tests.gpu_common import sample_rows
+
+    m, n, k = 2048, 4096, 11008
+    blocks = inputs.q6k_blocks(n, k, 8)
+    x = inputs.activations(m, k, 8, "silu_mul")
+    packed = q4k.q6k_pack_weights(to_dev(blocks), n, k)
+    y = q4k.q6k_gemm(packed, n, k, to_dev(x), out_dtype="bf16")
+    torch.cuda.synchronize()
+    rows = sample_rows(m, 4, 8)
+    want, scale = _oracle(blocks, x[rows])
+    assert_close(y.float().cpu().double().numpy()[rows], want, scale, "bf16", "q6k full size")
+
+
+def test_small_m_too_large_for_shared_memory_takes_tensor_path(q4k):
+    """16 tokens x 14336 do not fit the small-M kernel's shared memory: the
+    call takes the tensor-core path instead and stays correct."""
+    _check(q4k, 256, 14336, 16, 3, out="f32", act="f32")
