@@ -45,6 +45,9 @@ WORKLOADS = {
     "ffn": (2048, [(11008, 4096), (11008, 4096), (4096, 11008)], "bf16",
             "7B FFN linears gate/up 11008x4096 + down 4096x11008 Q4_K, 2048 tokens, fused q8, bf16 out"),
     "qproj2630": (2630, [(4096, 4096)], "bf16", "7B q-proj 4096x4096 Q4_K, 2630 tokens (outlier channels), fused q8, bf16 out"),
+    "down_q6k": (2048, [(4096, 11008)] * 8, "bf16",
+                 "7B down projection 4096x11008 with Q6_K weights (as Q4_K_M models store it), 2048 tokens, "
+                 "8 distinct matrices and inputs per step, fused q8, bf16 out (tensor-core path)"),
     "qproj512": (512, [(4096, 4096)], "f32", "7B q-proj 4096x4096 Q4_K, 512 tokens, fused q8, fp32 out"),
     "ffn_swiglu": (2048, [(22016, 4096), (4096, 11008)], "bf16",
                    "7B FFN with the SiLU(gate)*up epilogue: gate+up 11008x4096 as one pair GEMM whose epilogue "
@@ -61,6 +64,15 @@ WORKLOADS = {
                     "7B FFN gate projection 11008x4096 Q4_K at decode size: 1 token, fused q8, bf16 out "
                     "(small-M path, CUDA-graph replay)"),
 }
+
+
+def gemm_launches(m, n, k, sms):
+    """Kernels one prefill projection launches: the activation quantization,
+    the GEMM and, when the last wave of tiles is split along k, the fixup."""
+    tiles = -(-m // 128) * (n // 128)
+    rem = tiles % sms
+    split = rem > 0 and min(sms // rem, k // 256) >= 2
+    return 3 if split else 2
 
 
 def load_peaks():
@@ -109,17 +121,24 @@ def cpu_baseline(workload, seconds=10.0):
     import numpy as np
 
     from oracle import gemm as ogemm
-    from oracle import q4k_blocks, q8 as oq8
+    from oracle import q4k_blocks, q6k_blocks, q8 as oq8
     from quantized_prefill_gemm_gb300 import inputs
 
     tokens, mats, _, _ = WORKLOADS[workload]
     n, k, t = 4096, 4096, 32
-    fields = q4k_blocks.decode(inputs.q4k_blocks(n, k, 99))
+    q6 = workload in ("decode_q6k", "down_q6k")
+    if q6:
+        fields = q6k_blocks.decode(inputs.q6k_blocks(n, k, 99))
+    else:
+        fields = q4k_blocks.decode(inputs.q4k_blocks(n, k, 99))
     x = inputs.activations(t, k, 99)
     reps, t0 = 0, time.perf_counter()
     while True:
         qa, da, ss = oq8.quantize_rows(x)
-        ogemm.gemm_blockwise(fields, qa, da, ss)
+        if q6:
+            q6k_blocks.gemm_blockwise(fields, qa, da)
+        else:
+            ogemm.gemm_blockwise(fields, qa, da, ss)
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
@@ -133,7 +152,7 @@ def cpu_baseline(workload, seconds=10.0):
     except Exception:
         cores = os.cpu_count()
     return {"value": tokens / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{t} tokens x one 4096x4096 Q4_K matrix (numpy fp64 oracle: q8 quantization + blockwise "
+            "sample": f"{t} tokens x one 4096x4096 {'Q6_K' if q6 else 'Q4_K'} matrix (numpy fp64 oracle: q8 quantization + blockwise "
                       f"GEMM), {reps} repeats in {time.perf_counter() - t0:.1f} s, scaled by weight count "
                       f"({scale:.1f}x) and tokens ({tokens // t}x) to the workload"}, step_s
 
@@ -185,12 +204,13 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     tokens, mats, out, desc = WORKLOADS[args.workload]
+    sms = min(torch.cuda.get_device_properties(dev).multi_processor_count, 160)
     if args.workload == "ffn_swiglu":
         return run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local)
     kind = "outlier" if args.workload == "qproj2630" else "normal"
     # weights (packed once, resident) and one activation matrix per projection
     packed, xs, ys = [], [], []
-    q6 = args.workload == "decode_q6k"
+    q6 = args.workload in ("decode_q6k", "down_q6k")
     for i, (n, k) in enumerate(mats):
         if q6:
             blocks = inputs.q6k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
@@ -211,10 +231,15 @@ def main():
 
     def step(events=None):
         for i, (n, k) in enumerate(mats):
-            q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
-            if events is not None:
-                events[i][0].record(stream)
-            q4k.q4k_gemm_quantized(packed[i], n, k, ws, tokens, out, y=ys[i], stream=stream)
+            if q6:   # q6k_gemm quantizes into ws (bf16 operand) and runs the GEMM: the events take both
+                if events is not None:
+                    events[i][0].record(stream)
+                q4k.q6k_gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws, stream=stream)
+            else:
+                q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
+                if events is not None:
+                    events[i][0].record(stream)
+                q4k.q4k_gemm_quantized(packed[i], n, k, ws, tokens, out, y=ys[i], stream=stream)
             if events is not None:
                 events[i][1].record(stream)
 
@@ -258,14 +283,16 @@ def main():
     # launches of one stack step (ncu capture of this kernel version, summarized under profiles/)
     traffic = 49.35e6 if args.workload == "stack" else None
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic, "traffic_unit": "bytes per launch", "kernel": "q4k_gemm_kernel",
+                "traffic": traffic, "traffic_unit": "bytes per launch",
+                "kernel": "q4k_gemm_kernel" + ("<Q6_K>" if q6 else ""),
                 "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step); the GEMM issues "
                                "f16 tcgen05 MMAs, same rate class",
                 "per_launch": "2*M*N*K algorithmic flops / CUDA-event duration of each GEMM launch"}
 
     e2e = None
     if not args.no_e2e and rank == 0:
-        e2e = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream)
+        e2e = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream,
+                      gemm=q4k.q6k_gemm if q6 else None)
 
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -274,7 +301,8 @@ def main():
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
                        "l2": "inputs larger than L2 (whole step touches >18 GB)", "parallelism": f"replicas x{world}"},
             "effective_tops": eff_tops, "gemm_ms_per_step": gemm_ms / args.steps,
-            "roofline": roofline, "clocks": clk, "gpu_launches": 2 * len(mats) * args.steps}
+            "roofline": roofline, "clocks": clk,
+            "gpu_launches": sum(gemm_launches(tokens, n, k, sms) for n, k in mats) * args.steps}
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
@@ -424,7 +452,7 @@ def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, s
             "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ms, "steps": steps}
 
 
-def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2):
+def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2, gemm=None):
     """Same metric through the public fused call q4k_gemm, with every
     projection's activations copied from pinned host memory and its result
     copied back inside the timed region.  As a serving loop would, the copies
@@ -458,7 +486,7 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2)
             arrived.record(h2d)
             stream.wait_event(arrived)
             stream.wait_event(y_free[n][by])
-            q4k.q4k_gemm(packed[i], n, k, xb, out_dtype=out, y=yb, workspace=ws, stream=stream)
+            (gemm or q4k.q4k_gemm)(packed[i], n, k, xb, out_dtype=out, y=yb, workspace=ws, stream=stream)
             x_free[k][bx].record(stream)
             done = torch.cuda.Event()
             done.record(stream)
