@@ -295,29 +295,33 @@ __device__ __forceinline__ void convert_q6(const Ctx<kQ6>& cx, int s, int r, uin
     const uint8_t* scs = cx.sbase + L::kOffSc + L::kStageSc * s;
     uint8_t* bhi = cx.sbase + L::kOffB + L::kStageB * s + row_off;
     uint8_t* blo = bhi + L::kStageB / 2;
+    const __nv_bfloat162 m160 = __float2bfloat162_rn(-160.0f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const uint4 wl = *reinterpret_cast<const uint4*>(lo + (h * 128 + r) * 16);
         const uint2 wh = *reinterpret_cast<const uint2*>(hi + (h * 128 + r) * 8);
         const uint32_t scp = *reinterpret_cast<const uint16_t*>(scs + (h * 128 + r) * 2);
-        const float sc0 = static_cast<float>(static_cast<int8_t>(scp & 0xFFu));
-        const float sc1 = static_cast<float>(static_cast<int8_t>(scp >> 8));
+        // the scales as bf16 pairs (exact: |sc| <= 128)
+        const __nv_bfloat162 sc0 = __float2bfloat162_rn(static_cast<float>(static_cast<int8_t>(scp & 0xFFu)));
+        const __nv_bfloat162 sc1 = __float2bfloat162_rn(static_cast<float>(static_cast<int8_t>(scp >> 8)));
         const uint32_t lw[4] = {wl.x, wl.y, wl.z, wl.w};
         const uint32_t hw[4] = {wh.x, wh.x >> 2, wh.y, wh.y >> 2};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {   // 8-k group i of chunk h
-            uint32_t v[2];
-            unpack_q6(lw[i], hw[i], v[0], v[1]);
-            const float sc = i < 2 ? sc0 : sc1;
+            // q (0..63) per byte: low nibble, high bits, and u ^ 32 undone
+            uint32_t l0, l1, h0, h1;
+            unpack_group(lw[i], l0, l1);
+            unpack_group(hw[i] & 0x33333333u, h0, h1);
+            const uint32_t q[2] = {(l0 | (h0 << 4)) ^ 0x20202020u, (l1 | (h1 << 4)) ^ 0x20202020u};
+            const __nv_bfloat162 sc = i < 2 ? sc0 : sc1;
             uint32_t ohi[4], olo[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const uint32_t w = v[jj >> 1] >> (16 * (jj & 1));
-                const float a0 = static_cast<float>(static_cast<int8_t>(w & 0xFFu)) * sc;
-                const float a1 = static_cast<float>(static_cast<int8_t>((w >> 8) & 0xFFu)) * sc;
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-                const float2 hf = __bfloat1622float2(h2);
-                const __nv_bfloat162 l2 = __floats2bfloat162_rn(__fsub_rn(a0, hf.x), __fsub_rn(a1, hf.y));
+                // bf16 pair 128 + q (byte q under the exponent byte 0x43), minus 160: v = q - 32, exact
+                const uint32_t raw = __byte_perm(q[jj >> 1], 0x43434343u, (jj & 1) ? 0x4342u : 0x4140u);
+                const __nv_bfloat162 v = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&raw), m160);
+                const __nv_bfloat162 h2 = __hmul2(v, sc);                 // hi = RN_bf16(sc * v)
+                const __nv_bfloat162 l2 = __hfma2(v, sc, __hneg2(h2));    // lo = sc * v - hi, exact
                 ohi[jj] = *reinterpret_cast<const uint32_t*>(&h2);
                 olo[jj] = *reinterpret_cast<const uint32_t*>(&l2);
             }
