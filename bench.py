@@ -66,6 +66,25 @@ WORKLOADS = {
 }
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (the job's step time is its slowest
+    replica's); the ranks then meet at a barrier.  Without a process group it
+    is the value itself."""
+    if not dist:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def replica_seed(rank):
+    """Each replica draws its own weights and activations."""
+    return 4 + rank
+
+
 def gemm_launches(m, n, k, sms):
     """Kernels one prefill projection launches: the activation quantization,
     the GEMM and, when the last wave of tiles is split along k, the fixup."""
@@ -213,14 +232,14 @@ def main():
     q6 = args.workload in ("decode_q6k", "down_q6k")
     for i, (n, k) in enumerate(mats):
         if q6:
-            blocks = inputs.q6k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
+            blocks = inputs.q6k_blocks_torch(n, k, seed=replica_seed(rank), tag=i, device=dev)
             packed.append(q4k.q6k_pack_weights(blocks, n, k))
         else:
-            blocks = inputs.q4k_blocks_torch(n, k, seed=4 + rank, tag=i, device=dev)
+            blocks = inputs.q4k_blocks_torch(n, k, seed=replica_seed(rank), tag=i, device=dev)
             packed.append(q4k.q4k_pack_weights(blocks, n, k))
         del blocks
         kind_i = "silu_mul" if (args.workload == "ffn" and i == 2) else kind
-        xs.append(inputs.activations_torch(tokens, k, seed=4 + rank, kind=kind_i, tag=i, device=dev))
+        xs.append(inputs.activations_torch(tokens, k, seed=replica_seed(rank), kind=kind_i, tag=i, device=dev))
         ys.append(torch.empty((tokens, n), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device=dev))
     ws_bytes = max(q4k.q4k_act_workspace_bytes(tokens, k) for _, k in mats)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -261,12 +280,7 @@ def main():
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(stop)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
+    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
     ms_step = total_ms / args.steps
     gemm_ms = sum(a.elapsed_time(b) for s in ev for (a, b) in s)
     flops_step = sum(2.0 * tokens * n * k for n, k in mats)
@@ -320,14 +334,14 @@ def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
     from it.  roofline: both GEMMs' 2*M*N*K flops / their CUDA-event time."""
     tokens, mats, out, desc = WORKLOADS[args.workload]
     nf, k = 11008, 4096
-    gate = inputs.q4k_blocks_torch(nf, k, seed=4 + rank, tag=0, device=dev)
-    up = inputs.q4k_blocks_torch(nf, k, seed=4 + rank, tag=1, device=dev)
+    gate = inputs.q4k_blocks_torch(nf, k, seed=replica_seed(rank), tag=0, device=dev)
+    up = inputs.q4k_blocks_torch(nf, k, seed=replica_seed(rank), tag=1, device=dev)
     pair = q4k.q4k_pack_swiglu_weights(gate, up, nf, k)
     del gate, up
-    down_blocks = inputs.q4k_blocks_torch(4096, nf, seed=4 + rank, tag=2, device=dev)
+    down_blocks = inputs.q4k_blocks_torch(4096, nf, seed=replica_seed(rank), tag=2, device=dev)
     down = q4k.q4k_pack_weights(down_blocks, 4096, nf)
     del down_blocks
-    x = inputs.activations_torch(tokens, k, seed=4 + rank, kind="normal", tag=0, device=dev)
+    x = inputs.activations_torch(tokens, k, seed=replica_seed(rank), kind="normal", tag=0, device=dev)
     ws = torch.empty(q4k.q4k_act_workspace_bytes(tokens, k), dtype=torch.uint8, device=dev)
     h_ws = torch.empty(q4k.q4k_act_workspace_bytes(tokens, nf), dtype=torch.uint8, device=dev)
     y = torch.empty((tokens, 4096), dtype=torch.bfloat16, device=dev)
@@ -357,12 +371,7 @@ def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
     stop.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(stop)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
+    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
     err = q4k.q4k_device_error_word()
     if err:
         raise RuntimeError(f"device error word 0x{err:x}")
@@ -575,11 +584,7 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
     torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
     ms_products = timed(graphs["products"], args.steps)
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-        dist.barrier()
+    ms_step = max_over_ranks(ms_step, dist, dev)
     err = q4k.q4k_device_error_word()
     if err:
         raise RuntimeError(f"device error word 0x{err:x}")
