@@ -300,7 +300,7 @@ def main():
                 "traffic": traffic, "traffic_unit": "bytes per launch",
                 "kernel": "q4k_gemm_kernel" + ("<Q6_K>" if q6 else ""),
                 "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step); the GEMM issues "
-                               "f16 tcgen05 MMAs, same rate class",
+                               + ("bf16" if q6 else "f16") + " tcgen05 MMAs, same rate class",
                 "per_launch": "2*M*N*K algorithmic flops / CUDA-event duration of each GEMM launch"}
 
     e2e = None
@@ -310,8 +310,10 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers",
-            "data": "synthetic (seeded random Q4_K weights and activations)",
+            "vs_baseline": None,
+            "dtype": ("bf16 x bf16 -> f32 tensor-core MMA on exact q6/q8 integers (hi/lo weight planes)" if q6
+                      else "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers"),
+            "data": "synthetic (seeded random {} weights and activations)".format("Q6_K" if q6 else "Q4_K"),
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
                        "l2": "inputs larger than L2 (whole step touches >18 GB)", "parallelism": f"replicas x{world}"},
             "effective_tops": eff_tops, "gemm_ms_per_step": gemm_ms / args.steps,
@@ -603,8 +605,9 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
     desc = WORKLOADS[args.workload][3]
     line = {"metric": METRIC, "value": world * tokens / (ms_step * 1e-3), "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a on exact q4/q8 integers, fp32 rescale",
-            "data": "synthetic (seeded random Q4_K weights and activations)",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 dp4a on exact {}/q8 integers, fp32 rescale".format("q6" if q6 else "q4"),
+            "data": "synthetic (seeded random {} weights and activations)".format("Q6_K" if q6 else "Q4_K"),
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
                        "l2": f"{weights_gb:.2f} GB of weights per step" + (
                            " (larger than L2)" if weights_gb > 0.2 else " (L2-resident between replays)"),
