@@ -19,19 +19,23 @@
 // hi/lo splits of both operands (three MMAs: hi*hi + hi*lo + lo*hi, relative
 // error ~2^-16 per term, far inside the 1e-4 * sum|w*a| bound).
 //
-// One persistent CTA per SM (448 threads, 14 warps), one 128-token x 128-od
+// One persistent CTA per SM (512 threads, 16 warps), one 128-token x 128-od
 // output tile at a time, k in stages of 64 (2 chunks of 32):
 //   warp 0        TMA producer: activation tile (fp16, 128-B swizzle), packed
 //                 quants, sc, da, d; for the min-term stages the bf16 E and
 //                 -(dmin*m) tiles
-//   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk into one of two
-//                 TMEM accumulators; 4 bf16 MMAs per min-term stage into the
-//                 tile's Y accumulator
-//   warps 2-5     converters: 4-bit quants -> fp16 sc*q written in the
+//   warp 1        MMA issuer: per main stage 2 x (M128 N128 K16) per chunk into
+//                 the two accumulators of one TMEM group, one commit for both;
+//                 4 bf16 MMAs per min-term stage into a group's first one
+//   warps 2-3     no role (they complete the first warpgroup)
+//   warps 4-7     converters: 4-bit quants -> fp16 sc*q written in the
 //                 128-B-swizzled K-major layout the MMA reads
-//   warps 6-13    epilogue: per chunk, P += da * J (packed fp32 FMA) from
-//                 TMEM; per super-block Y += d * P in TMEM; per tile Y -> HBM
-// TMEM (512 columns): J buffers at 0 and 128, Y buffers at 256 and 384.
+//   warps 8-15    drain: per chunk, P += da * J (packed fp32 FMA) from TMEM;
+//                 per super-block Y += d * P; per tile Y -> HBM.  Y and P live
+//                 in registers (setmaxnreg gives these warps 184 each).
+// TMEM (512 columns): two groups of two 128-column accumulators.  A group is
+// handed over once per 64-k stage, which halves the MMA <-> drain hand-offs
+// of a per-chunk scheme; those hand-offs, not the tensor pipe, bound the loop.
 // Every wait is bounded (q4k_ptx.cuh: mbar_wait): a stuck pipeline records an
 // error word and the CTA leaves through the normal teardown.
 #include <cuda_bf16.h>
@@ -45,7 +49,7 @@
 namespace q4k {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 
 // Shared-memory carve-out per format.  Q4_K: five stages of the fp16 A tile,
 // the fp16 B tile (sc*q), the packed quants, sc, d_a and d.  Q6_K: four stages
@@ -72,17 +76,21 @@ struct Lay {
     static constexpr int kBarFull = 0;                       // [kStages] producer -> all (tx bytes)
     static constexpr int kBarConv = kStages;                 // [kStages] converters -> MMA (4 arrivals)
     static constexpr int kBarEmpty = 2 * kStages;            // [kStages] MMA commit + 8 epilogue warps -> producer
-    static constexpr int kBarAccFull = 3 * kStages;          // [2] MMA commit -> epilogue
-    static constexpr int kBarAccEmpty = kBarAccFull + 2;     // [2] 8 epilogue warps -> MMA
-    static constexpr int kBarZ = kBarAccEmpty + 2;           // [2] MMA commit (min term done) -> epilogue
-    static constexpr int kBarYEmpty = kBarZ + 2;             // [2] 8 epilogue warps -> MMA
-    static constexpr int kBarDrain = kBarYEmpty + 2;         // MMA's final commit
+    static constexpr int kBarAccFull = 3 * kStages;          // [2] MMA commit -> drain (one accumulator group)
+    static constexpr int kBarAccEmpty = kBarAccFull + 2;     // [2] 8 drain warps -> MMA
+    static constexpr int kBarDrain = kBarAccEmpty + 2;       // MMA's final commit
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
     static constexpr size_t kSmemBytes = kSmemUsed + 1024;          // + alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
+
+// Per-thread registers after the re-split (warpgroups 0, 1 and 2-3).  The
+// launch gives every thread 65536 / 512 = 128; the shares must not add up to
+// more than that total, or the increase would wait forever.
+constexpr uint32_t kRegsCtl = 56, kRegsConv = 80, kRegsDrain = 184;
+static_assert(128 * kRegsCtl + 128 * kRegsConv + 256 * kRegsDrain <= 65536, "register re-split exceeds the launch");
 
 constexpr uint32_t kIdescMain = idesc_kind_f16(128, 128, false);   // fp16 x fp16 -> fp32
 constexpr uint32_t kIdescMin = idesc_kind_f16(128, 128, true);     // bf16 x bf16 -> fp32
@@ -209,50 +217,56 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
 }
 
 // ----------------------------------------------------------- MMA issuer --
+// TMEM holds four 128-column accumulators in two groups (group g: columns
+// 256 g .. 256 g + 255).  One group use is one 64-k main stage (chunk h of
+// the stage accumulates into column 256 g + 128 h) or, at the start of a unit
+// with min-term stages, all of its min-term stages (Z accumulates into the
+// group's first accumulator).  One commit hands a whole group to the drain,
+// and the drain hands it back with one arrival per warp.
 template <bool kQ6>
 __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p) {
     using L = Lay<kQ6>;
-    int s = 0, ab = 0, it = 0;
-    uint32_t ph = 0, aph = 0;
+    int s = 0, g = 0;
+    uint32_t ph = 0, gph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
-        const int yb = it & 1;
-        const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
-        if (!cx.wait(p, L::kBarYEmpty + yb, yph ^ 1u, kSiteMmaYEmpty)) break;
-        tc_fence_after();
-        const uint32_t ty = cx.tmem + 256u + 128u * yb;
-        // a unit without min-term stages still completes the buffer's Z phase
-        // (nothing to wait for: the epilogue starts Y at zero itself)
-        if (w.kbase >= 0) tc_commit(cx.bar(L::kBarZ + yb));
         for (int st = 0; st < w.n_st; ++st) {
+            const int kb = st + w.kbase;
+            if ((kb >= 0 || st == 0) && !cx.wait(p, L::kBarAccEmpty + g, gph ^ 1u, kSiteMmaAccEmpty)) {
+                ok = false;
+                break;
+            }
             if (!cx.wait(p, L::kBarFull + s, ph, kSiteMmaFull)) {
                 ok = false;
                 break;
             }
+            // the converters' arrival is awaited on every stage, min-term stages
+            // included: a stage is then never refilled before they have passed it
+            if (!cx.wait(p, L::kBarConv + s, ph, kSiteMmaConv)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
             const uint64_t ad = sw128_kmajor_desc(cx.a(s));
             const uint64_t bd = sw128_kmajor_desc(cx.b(s));
-            if (st + w.kbase < 0) {
-                tc_fence_after();
+            const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
+            if (kb < 0) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
-                    tc_mma_f16(ty, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
+                    tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
                 tc_commit(cx.bar(L::kBarEmpty + s));
-                if (st + w.kbase == -1) tc_commit(cx.bar(L::kBarZ + yb));
-            } else {
-                if (!cx.wait(p, L::kBarConv + s, ph, kSiteMmaConv)) {
-                    ok = false;
-                    break;
+                if (kb == -1) {   // Z complete: the group goes to the drain
+                    tc_commit(cx.bar(L::kBarAccFull + g));
+                    if (++g == 2) {
+                        g = 0;
+                        gph ^= 1u;
+                    }
                 }
-                tc_fence_after();
+            } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // the two 32-k chunks of this stage
-                    if (!cx.wait(p, L::kBarAccEmpty + ab, aph ^ 1u, kSiteMmaAccEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t tj = cx.tmem + 128u * ab;
+                    const uint32_t tj = tg + 128u * h;
                     if constexpr (kQ6) {   // bf16: the hi plane, then the lo plane, into one accumulator
                         const uint64_t bl = sw128_kmajor_desc(cx.b(s) + L::kStageB / 2);
                         tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMin, 0u);
@@ -263,14 +277,13 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                         tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
                         tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
                     }
-                    tc_commit(cx.bar(L::kBarAccFull + ab));
-                    if (++ab == 2) {
-                        ab = 0;
-                        aph ^= 1u;
-                    }
                 }
-                if (!ok) break;
+                tc_commit(cx.bar(L::kBarAccFull + g));
                 tc_commit(cx.bar(L::kBarEmpty + s));
+                if (++g == 2) {
+                    g = 0;
+                    gph ^= 1u;
+                }
             }
             advance<kQ6>(s, ph);
         }
@@ -401,10 +414,9 @@ __device__ __forceinline__ void run_converter(const Ctx<kQ6>& cx, const GemmPara
 }
 
 // -------------------------------------------------------------- epilogue --
-// The epilogue works on 16-column pieces (tcgen05.ld/st .x16) to keep its
-// live registers (64 partial sums + one 16-value piece) within the budget
-// of a 448-thread CTA.
-__device__ __forceinline__ void store_row16(const GemmParams& p, int64_t t, int col, const uint32_t (&v)[16]) {
+// The drain keeps the tile's running Y and the super-block's partial sums P
+// in registers (64 + 64 per thread: a token row and 64 output columns).
+__device__ __forceinline__ void store_row16(const GemmParams& p, int64_t t, int col, const float* v) {
     if (p.out_bf16) {
         __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + t * p.ldy + col;
 #pragma unroll
@@ -412,8 +424,7 @@ __device__ __forceinline__ void store_row16(const GemmParams& p, int64_t t, int 
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 pr =
-                    __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * i]), __uint_as_float(v[8 * q + 2 * i + 1]));
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
                 w[i] = *reinterpret_cast<const uint32_t*>(&pr);
             }
             *reinterpret_cast<uint4*>(y + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -421,8 +432,7 @@ __device__ __forceinline__ void store_row16(const GemmParams& p, int64_t t, int 
     } else {
         float* y = static_cast<float*>(p.y) + t * p.ldy + col;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(y + 4 * q) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<float4*>(y + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
 }
 
@@ -468,22 +478,18 @@ __device__ __forceinline__ float silu_mul_fixed(float g, float u) {
 }
 
 // Tile end of the gate/up pair GEMM: this thread holds, for token t, the 32
-// gate outputs (TMEM columns 0-31 of its 64) and the 32 up outputs of the same
-// features (columns 32-63).  It forms h, quantizes it as one 32-element q8
+// gate outputs (its columns 0-31) and the 32 up outputs of the same features
+// (columns 32-63).  It forms h, quantizes it as one 32-element q8
 // block (chunk c of the down projection's input; the same rule as
 // q8_quantize_rows: d = RN(amax/127), inv = RN(127/amax),
 // qa = clamp(rint_even(RN(h*inv)), -127, 127), d_a = RN16(d), a block with
 // amax < 2^-120 is zero) and writes the down projection's operand: fp16 qa,
 // fp32 d_a and the hi/lo bf16 split of d_a*ssum.
-__device__ __forceinline__ void swiglu_store(const GemmParams& p, int64_t t, int c, const uint32_t (&g0)[16],
-                                             const uint32_t (&g1)[16], const uint32_t (&u0)[16],
-                                             const uint32_t (&u1)[16]) {
+__device__ __forceinline__ void swiglu_store(const GemmParams& p, int64_t t, int c, const float* gate,
+                                             const float* up) {
     float h[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        h[i] = silu_mul_fixed(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
-        h[16 + i] = silu_mul_fixed(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
-    }
+    for (int i = 0; i < 32; ++i) h[i] = silu_mul_fixed(gate[i], up[i]);
     float amax = fabsf(h[0]);
 #pragma unroll
     for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
@@ -515,124 +521,114 @@ __device__ __forceinline__ void swiglu_store(const GemmParams& p, int64_t t, int
     p.he[(static_cast<int64_t>(p.m) + t) * p.hkc + c] = lo;
 }
 
-__device__ __forceinline__ void dump_chunk(const GemmParams& p, int64_t t, int col, int64_t c, const uint32_t (&J)[16]) {
-    if (t >= p.m) return;
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) p.dbg[(t * p.n + col + j) * p.kc + c] = __uint_as_float(J[j]);
+// A k-part of a split tile: this warp's 32 x 64 slice of the partial Y to the
+// workspace, for the fixup kernel.
+__device__ __forceinline__ void store_partial(const GemmParams& p, const float* Y, int slot, int slice, int lane) {
+    float4* dst = reinterpret_cast<float4*>(p.part + ((static_cast<int64_t>(slot) * 8 + slice) * 32 + lane) * 64);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) dst[i] = make_float4(Y[4 * i], Y[4 * i + 1], Y[4 * i + 2], Y[4 * i + 3]);
 }
 
-// Warp e (0..7) reads TMEM lanes 32*(warp%4)..+31 (the lane quadrant its
-// warp index allows) and columns 64*(e/4)..+63 of each buffer: each thread
-// owns one token row and 64 output columns.
-// A k-part of a split tile: this warp's 32 x 64 slice of the partial Y (TMEM
-// at ty) to the workspace, for the fixup kernel.  Kept out of line: the
-// epilogue loop's register allocation then stays that of whole tiles.
-__device__ __noinline__ void store_partial(const GemmParams& p, uint32_t ty, int slot, int slice, int lane) {
-    float* dst = p.part + ((static_cast<int64_t>(slot) * 8 + slice) * 32 + lane) * 64;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t Yv[16];
-        tmem_ld16(ty + 16u * q, Yv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            reinterpret_cast<uint4*>(dst + 16 * q)[i] = make_uint4(Yv[4 * i], Yv[4 * i + 1], Yv[4 * i + 2], Yv[4 * i + 3]);
-    }
-}
-
+// Drain warp e (0..7) reads TMEM lanes 32*(warp%4)..+31 (the lane quadrant
+// its warp index allows) and columns 64*(e/4)..+63 of each accumulator: each
+// thread owns one token row and 64 output columns.  Per main stage it folds
+// both chunks, P += d_a * J (packed fp32 FMA), and hands the group back after
+// its last TMEM load; per super-block Y += d * P; per unit Y -> HBM.
 template <bool kDump, bool kSwiGLU, bool kQ6>
 __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParams& p, int warp, int e, int lane) {
     using L = Lay<kQ6>;
     const int qd = warp & 3, ch = e >> 2;
     const int row = qd * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    int s = 0, ab = 0, it = 0;
-    uint32_t ph = 0, aph = 0;
+    int s = 0, g = 0;
+    uint32_t ph = 0, gph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
         const int mt = w.mt, nt = w.nt;
-        const int yb = it & 1;
-        const uint32_t yph = static_cast<uint32_t>(it >> 1) & 1u;
-        const uint32_t ty = cx.tmem + lane_off + 256u + 128u * yb + 64u * ch;
         const int64_t t = static_cast<int64_t>(mt) * 128 + row;
         const int col0 = nt * 128 + 64 * ch;
-        float P[64];
+        float Y[64], P[64];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) P[j] = 0.0f;
-        bool zready = false;
-        if (w.kbase >= 0) {   // no min-term stages write Y: start it at zero
-            uint32_t z[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) z[j] = 0u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_st16(ty + 16u * q, z);
-            tmem_wait_st();
+        for (int j = 0; j < 64; ++j) {
+            Y[j] = 0.0f;   // a unit without min-term stages starts at zero
+            P[j] = 0.0f;
         }
-        for (int st = 0; ok && st < w.n_st; ++st) {
+        for (int st = 0; st < w.n_st; ++st) {
             if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteEpiFull)) {
                 ok = false;
                 break;
             }
             const int kb = st + w.kbase;
-            if (kb >= 0) {
+            if (kb == -1) {   // the min-term group is complete: Y starts at Z
+                if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiZ)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tz = cx.tmem + lane_off + 256u * static_cast<uint32_t>(g) + 64u * ch;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t Z[16];
+                    tmem_ld16(tz + 16u * q, Z);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) Y[16 * q + j] = __uint_as_float(Z[j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + g));
+                if (++g == 2) {
+                    g = 0;
+                    gph ^= 1u;
+                }
+            } else if (kb >= 0) {
                 const float* das = reinterpret_cast<const float*>(cx.sbase + L::kOffDa + L::kStageDa * s);
+                const float da0 = das[row], da1 = das[128 + row];
+                if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiAccFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tg = cx.tmem + lane_off + 256u * static_cast<uint32_t>(g) + 64u * ch;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float da = das[h * 128 + row];
-                    if (ok && !cx.warp_wait(p, L::kBarAccFull + ab, aph, kSiteEpiAccFull)) ok = false;
-                    if (ok) {
-                        tc_fence_after();
-                        const uint32_t tj = cx.tmem + lane_off + 128u * ab + 64u * ch;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t J[16];
-                            tmem_ld16(tj + 16u * q, J);
-                            tmem_wait_ld();
-                            if (q == 3) {   // whole buffer read: hand it back to the MMA
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + ab));
-                            }
-#pragma unroll
-                            for (int j = 0; j < 16; j += 2)
-                                ffma2(P[16 * q + j], P[16 * q + j + 1], da, da, __uint_as_float(J[j]),
-                                      __uint_as_float(J[j + 1]));
-                            if (kDump) dump_chunk(p, t, col0 + 16 * q, 2 * kb + h, J);
-                        }
-                    }
-                    if (++ab == 2) {
-                        ab = 0;
-                        aph ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                if ((kb & 3) == 3) {   // super-block done: Y += d * P
-                    if (!zready) {
-                        if (!cx.warp_wait(p, L::kBarZ + yb, yph, kSiteEpiZ)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        zready = true;
-                    }
-                    const float* dv = reinterpret_cast<const float*>(cx.sbase + L::kOffD + L::kStageD * s) + 64 * ch;
+                    const float da = h ? da1 : da0;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint32_t Yv[16];
-                        tmem_ld16(ty + 16u * q, Yv);
+                        uint32_t J[16];
+                        tmem_ld16(tg + 128u * h + 16u * q, J);
                         tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 d4 = *reinterpret_cast<const float4*>(dv + 16 * q + j);
-                            Yv[j] = __float_as_uint(fmaf(d4.x, P[16 * q + j], __uint_as_float(Yv[j])));
-                            Yv[j + 1] = __float_as_uint(fmaf(d4.y, P[16 * q + j + 1], __uint_as_float(Yv[j + 1])));
-                            Yv[j + 2] = __float_as_uint(fmaf(d4.z, P[16 * q + j + 2], __uint_as_float(Yv[j + 2])));
-                            Yv[j + 3] = __float_as_uint(fmaf(d4.w, P[16 * q + j + 3], __uint_as_float(Yv[j + 3])));
+                        if (h == 1 && q == 3) {   // both accumulators read: the group goes back to the MMA
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + g));
                         }
-                        tmem_st16(ty + 16u * q, Yv);
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2)
+                            ffma2(P[16 * q + j], P[16 * q + j + 1], da, da, __uint_as_float(J[j]),
+                                  __uint_as_float(J[j + 1]));
+                        if (kDump && t < p.m) {
+#pragma unroll 4
+                            for (int j = 0; j < 16; ++j)
+                                p.dbg[(t * p.n + col0 + 16 * q + j) * p.kc + 2 * kb + h] = __uint_as_float(J[j]);
+                        }
                     }
-                    tmem_wait_st();
+                }
+                if (++g == 2) {
+                    g = 0;
+                    gph ^= 1u;
+                }
+                if ((kb & 3) == 3) {   // super-block done: Y += d * P
+                    const float* dv = reinterpret_cast<const float*>(cx.sbase + L::kOffD + L::kStageD * s) + 64 * ch;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(dv + j);
+                        Y[j] = fmaf(d4.x, P[j], Y[j]);
+                        Y[j + 1] = fmaf(d4.y, P[j + 1], Y[j + 1]);
+                        Y[j + 2] = fmaf(d4.z, P[j + 2], Y[j + 2]);
+                        Y[j + 3] = fmaf(d4.w, P[j + 3], Y[j + 3]);
+                    }
 #pragma unroll
                     for (int j = 0; j < 64; ++j) P[j] = 0.0f;
                 }
@@ -643,39 +639,18 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
         }
         if (!ok) break;
         if (w.slot >= 0) {   // a k-part of a split tile: its partial Y, finished by the fixup kernel
-            store_partial(p, ty, w.slot, qd * 2 + ch, lane);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(L::kBarYEmpty + yb));
+            store_partial(p, Y, w.slot, qd * 2 + ch, lane);
         } else if constexpr (kSwiGLU) {
-            // tile done: the 64 columns are 32 gate and 32 up outputs of the
-            // down projection's input chunk c = 2 nt + ch
-            uint32_t g0[16], g1[16], u0[16], u1[16];
-            tmem_ld16(ty, g0);
-            tmem_ld16(ty + 16u, g1);
-            tmem_ld16(ty + 32u, u0);
-            tmem_ld16(ty + 48u, u1);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(L::kBarYEmpty + yb));
+            // the 64 columns are 32 gate and 32 up outputs of the down
+            // projection's input chunk c = 2 nt + ch
             const int c = 2 * nt + ch;
             if (t < p.m)
-                swiglu_store(p, t, c, g0, g1, u0, u1);
+                swiglu_store(p, t, c, Y, Y + 32);
             else   // padding token of the last 128-token tile: scale 0
                 p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = 0.0f;
-        } else {
-            // tile done: Y (TMEM) -> HBM
+        } else if (t < p.m) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t Yv[16];
-                tmem_ld16(ty + 16u * q, Yv);
-                tmem_wait_ld();
-                if (t < p.m) store_row16(p, t, col0 + 16 * q, Yv);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(L::kBarYEmpty + yb));
+            for (int q = 0; q < 4; ++q) store_row16(p, t, col0 + 16 * q, Y + 16 * q);
         }
     }
 }
@@ -708,8 +683,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(cx.bar(L::kBarAccFull + b), 1);
             mbar_init(cx.bar(L::kBarAccEmpty + b), 8);
-            mbar_init(cx.bar(L::kBarZ + b), 1);
-            mbar_init(cx.bar(L::kBarYEmpty + b), 8);
         }
         mbar_init(cx.bar(L::kBarDrain), 1);
         *cx.abort_flag = 0;
@@ -730,16 +703,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // read, and Y or the workspace written, only after it has completed
     griddep_wait();
 
-    if (warp == 0) {
-        if (lane == 0) run_producer<kQ6>(cx, p, &tm_x, &tm_e, &tm_d);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) run_mma<kQ6>(cx, p);
-        __syncwarp();
-    } else if (warp < 6) {
-        run_converter<kQ6>(cx, p, warp - 2, lane);
+    // registers are re-split per warpgroup: the drain holds 128 live values
+    // per thread, the producer, MMA and converter roles need far fewer
+    if (warp < 4) {
+        regs_dec<kRegsCtl>();
+        if (warp == 0) {
+            if (lane == 0) run_producer<kQ6>(cx, p, &tm_x, &tm_e, &tm_d);
+            __syncwarp();
+        } else if (warp == 1) {
+            if (lane == 0) run_mma<kQ6>(cx, p);
+            __syncwarp();
+        }   // warps 2 and 3 have no role
+    } else if (warp < 8) {
+        regs_dec<kRegsConv>();
+        run_converter<kQ6>(cx, p, warp - 4, lane);
     } else {
-        run_epilogue<kDump, kSwiGLU, kQ6>(cx, p, warp, warp - 6, lane);
+        regs_inc<kRegsDrain>();
+        run_epilogue<kDump, kSwiGLU, kQ6>(cx, p, warp, warp - 8, lane);
     }
 
     tc_fence_before();
