@@ -62,20 +62,18 @@ struct Lay {
     static constexpr uint32_t kStageNib = 4096;                 // 2 chunks x 128 rows x 16 B
     static constexpr uint32_t kStageHi = kQ6 ? 2048 : 0;        // 2 chunks x 128 rows x 8 B
     static constexpr uint32_t kStageSc = kQ6 ? 512 : 256;       // 2 chunks x 128 rows x (2 or 1) B
-    static constexpr uint32_t kStageDa = 1024;                  // 2 chunks x 128 tokens x fp32
     static constexpr uint32_t kStageD = 512;                    // 128 rows x fp32 (last stage of a super-block)
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + kStages * kStageA;
     static constexpr uint32_t kOffNib = kOffB + kStages * kStageB;
     static constexpr uint32_t kOffHi = kOffNib + kStages * kStageNib;
     static constexpr uint32_t kOffSc = kOffHi + kStages * kStageHi;
-    static constexpr uint32_t kOffDa = kOffSc + kStages * kStageSc;
-    static constexpr uint32_t kOffD = kOffDa + kStages * kStageDa;
+    static constexpr uint32_t kOffD = kOffSc + kStages * kStageSc;
     static constexpr uint32_t kOffBar = kOffD + kStages * kStageD;
     // barrier indices
     static constexpr int kBarFull = 0;                       // [kStages] producer -> all (tx bytes)
     static constexpr int kBarConv = kStages;                 // [kStages] converters -> MMA (4 arrivals)
-    static constexpr int kBarEmpty = 2 * kStages;            // [kStages] MMA commit + 8 epilogue warps -> producer
+    static constexpr int kBarEmpty = 2 * kStages;            // [kStages] MMA commit + 8 drain arrivals -> producer
     static constexpr int kBarAccFull = 3 * kStages;          // [2] MMA commit -> drain (one accumulator group)
     static constexpr int kBarAccEmpty = kBarAccFull + 2;     // [2] 8 drain warps -> MMA
     static constexpr int kBarDrain = kBarAccEmpty + 2;       // MMA's final commit
@@ -188,7 +186,7 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
             } else {
                 const int kb = st + w.kbase;
                 const bool sb_last = (kb & 3) == 3;
-                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageNib + L::kStageHi + L::kStageSc + L::kStageDa +
+                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageNib + L::kStageHi + L::kStageSc +
                                               (sb_last ? L::kStageD : 0u));
                 tma_load_2d(cx.a(s), tm_x, fb, 64 * kb, 128 * mt);
                 const int64_t rec = static_cast<int64_t>(nt) * p.kc + 2 * kb;
@@ -199,8 +197,6 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
                 } else {
                     bulk_load(cx.base + L::kOffSc + L::kStageSc * s, p.sc + rec * 128, L::kStageSc, fb);
                 }
-                bulk_load(cx.base + L::kOffDa + L::kStageDa * s, p.da + (static_cast<int64_t>(mt) * p.kc + 2 * kb) * 128,
-                          L::kStageDa, fb);
                 if (sb_last)
                     bulk_load(cx.base + L::kOffD + L::kStageD * s,
                               p.dsb + (static_cast<int64_t>(nt) * p.ksb + (kb >> 2)) * 128, L::kStageD, fb);
@@ -256,6 +252,7 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                 for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
                     tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
                 tc_commit(cx.bar(L::kBarEmpty + s));
+                mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);   // the drain reads nothing of this stage
                 if (kb == -1) {   // Z complete: the group goes to the drain
                     tc_commit(cx.bar(L::kBarAccFull + g));
                     if (++g == 2) {
@@ -280,6 +277,9 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                 }
                 tc_commit(cx.bar(L::kBarAccFull + g));
                 tc_commit(cx.bar(L::kBarEmpty + s));
+                // the drain reads a stage (its d) only at the end of a super-block;
+                // for every other stage this thread arrives in its place
+                if ((kb & 3) != 3) mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);
                 if (++g == 2) {
                     g = 0;
                     gph ^= 1u;
@@ -533,7 +533,9 @@ __device__ __forceinline__ void store_partial(const GemmParams& p, const float* 
 // its warp index allows) and columns 64*(e/4)..+63 of each accumulator: each
 // thread owns one token row and 64 output columns.  Per main stage it folds
 // both chunks, P += d_a * J (packed fp32 FMA), and hands the group back after
-// its last TMEM load; per super-block Y += d * P; per unit Y -> HBM.
+// its last TMEM load; per super-block Y += d * P; per unit Y -> HBM.  Of the
+// stage ring it joins only the super-block ends (to read d): the MMA thread
+// arrives in its place on every other stage.
 template <bool kDump, bool kSwiGLU, bool kQ6>
 __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParams& p, int warp, int e, int lane) {
     using L = Lay<kQ6>;
@@ -554,11 +556,17 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
             Y[j] = 0.0f;   // a unit without min-term stages starts at zero
             P[j] = 0.0f;
         }
+        // d_a straight from global memory (this thread's token, two chunks per
+        // stage), loaded one main stage ahead so that its latency is hidden
+        const int kb_end = w.kbase + w.n_st;
+        const float* dap = p.da + static_cast<int64_t>(mt) * p.kc * 128 + row;   // + 128 * chunk
+        float da_n0 = 0.0f, da_n1 = 0.0f;
+        if (max(w.kbase, 0) < kb_end) {
+            const int c0 = 2 * max(w.kbase, 0);
+            da_n0 = __ldg(dap + 128 * c0);
+            da_n1 = __ldg(dap + 128 * (c0 + 1));
+        }
         for (int st = 0; st < w.n_st; ++st) {
-            if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteEpiFull)) {
-                ok = false;
-                break;
-            }
             const int kb = st + w.kbase;
             if (kb == -1) {   // the min-term group is complete: Y starts at Z
                 if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiZ)) {
@@ -583,8 +591,11 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
                     gph ^= 1u;
                 }
             } else if (kb >= 0) {
-                const float* das = reinterpret_cast<const float*>(cx.sbase + L::kOffDa + L::kStageDa * s);
-                const float da0 = das[row], da1 = das[128 + row];
+                const float da0 = da_n0, da1 = da_n1;
+                if (kb + 1 < kb_end) {
+                    da_n0 = __ldg(dap + 128 * (2 * kb + 2));
+                    da_n1 = __ldg(dap + 128 * (2 * kb + 3));
+                }
                 if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiAccFull)) {
                     ok = false;
                     break;
@@ -619,7 +630,11 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
                     g = 0;
                     gph ^= 1u;
                 }
-                if ((kb & 3) == 3) {   // super-block done: Y += d * P
+                if ((kb & 3) == 3) {   // super-block done: Y += d * P, d from this stage
+                    if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteEpiFull)) {
+                        ok = false;
+                        break;
+                    }
                     const float* dv = reinterpret_cast<const float*>(cx.sbase + L::kOffD + L::kStageD * s) + 64 * ch;
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
@@ -631,10 +646,10 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
                     }
 #pragma unroll
                     for (int j = 0; j < 64; ++j) P[j] = 0.0f;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(cx.bar(L::kBarEmpty + s));
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(L::kBarEmpty + s));
             advance<kQ6>(s, ph);
         }
         if (!ok) break;
