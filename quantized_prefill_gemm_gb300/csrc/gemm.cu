@@ -20,11 +20,12 @@
 // error ~2^-16 per term, far inside the 1e-4 * sum|w*a| bound).
 //
 // One persistent CTA per SM (512 threads, 16 warps), one 128-token x 128-od
-// output tile at a time, k in stages of 64 (2 chunks of 32):
+// output tile at a time, k in stages of 128 for Q4_K and 64 for Q6_K (four or
+// two chunks of 32):
 //   warp 0        TMA producer: activation tile (fp16, 128-B swizzle), packed
 //                 quants, sc, da, d; for the min-term stages the bf16 E and
 //                 -(dmin*m) tiles
-//   warp 1        MMA issuer: per main stage 2 x (M128 N128 K16) per chunk into
+//   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk, two chunks into
 //                 the two accumulators of one TMEM group, one commit for both;
 //                 4 bf16 MMAs per min-term stage into a group's first one
 //   warps 2-3     no role (they complete the first warpgroup)
@@ -34,7 +35,7 @@
 //                 per super-block Y += d * P; per tile Y -> HBM.  Y and P live
 //                 in registers (setmaxnreg gives these warps 184 each).
 // TMEM (512 columns): two groups of two 128-column accumulators.  A group is
-// handed over once per 64-k stage, which halves the MMA <-> drain hand-offs
+// handed over once per two chunks, which halves the MMA <-> drain hand-offs
 // of a per-chunk scheme; those hand-offs, not the tensor pipe, bound the loop.
 // Every wait is bounded (q4k_ptx.cuh: mbar_wait): a stuck pipeline records an
 // error word and the CTA leaves through the normal teardown.
@@ -51,17 +52,23 @@ namespace {
 
 constexpr int kThreads = 512;
 
-// Shared-memory carve-out per format.  Q4_K: five stages of the fp16 A tile,
-// the fp16 B tile (sc*q), the packed quants, sc, d_a and d.  Q6_K: four stages
-// (the B tile has two bf16 planes, hi and lo) plus the high quant bits.
+// Shared-memory carve-out per format.  Q4_K: three stages of 128 k (four
+// 32-k chunks) holding the fp16 A tile, the fp16 B tile (sc*q), the packed
+// quants, sc and d.  Q6_K: four stages of 64 k (the B tile has two bf16
+// planes, hi and lo) plus the high quant bits.  A and B tiles are made of
+// 16 KB boxes of 128 rows x 64 k (128-B rows, 128-B swizzle), one per two
+// chunks.  A min-term stage uses the first box of A and of B.
 template <bool kQ6>
 struct Lay {
-    static constexpr int kStages = kQ6 ? 4 : 5;
-    static constexpr uint32_t kStageA = 16384;                  // 128 rows x 64 fp16 / bf16
-    static constexpr uint32_t kStageB = kQ6 ? 32768 : 16384;    // Q6_K: hi plane, then lo plane
-    static constexpr uint32_t kStageNib = 4096;                 // 2 chunks x 128 rows x 16 B
-    static constexpr uint32_t kStageHi = kQ6 ? 2048 : 0;        // 2 chunks x 128 rows x 8 B
-    static constexpr uint32_t kStageSc = kQ6 ? 512 : 256;       // 2 chunks x 128 rows x (2 or 1) B
+    static constexpr int kCh = gemm_chunks_per_stage(kQ6);     // 32-k chunks per main stage
+    static constexpr int kStPerSb = 8 / kCh;                    // main stages per super-block
+    static constexpr int kStages = kQ6 ? 4 : 3;
+    static constexpr uint32_t kBox = 16384;                     // 128 rows x 64 fp16 / bf16
+    static constexpr uint32_t kStageA = kBox * (kCh / 2);
+    static constexpr uint32_t kStageB = kQ6 ? 2 * kBox : kBox * (kCh / 2);   // Q6_K: hi plane, then lo plane
+    static constexpr uint32_t kStageNib = 2048 * kCh;           // chunks x 128 rows x 16 B
+    static constexpr uint32_t kStageHi = kQ6 ? 1024 * kCh : 0;  // chunks x 128 rows x 8 B
+    static constexpr uint32_t kStageSc = (kQ6 ? 256 : 128) * kCh;   // chunks x 128 rows x (2 or 1) B
     static constexpr uint32_t kStageD = 512;                    // 128 rows x fp32 (last stage of a super-block)
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + kStages * kStageA;
@@ -130,7 +137,8 @@ __device__ __forceinline__ void advance(int& s, uint32_t& ph) {
 // One work unit: a whole tile, or one k-part of a tail tile (GemmParams).
 // Its stages st = 0 .. n_st-1 map to kb = st + kbase: kb < 0 are the
 // min-term stages (a unit has all of them or none: only whole tiles and part
-// 0 have them, and those start at kb = 0), kb >= 0 the 64-k main stages.
+// 0 have them, and those start at kb = 0), kb >= 0 the main stages of kCh
+// chunks.
 struct Unit {
     int mt, nt;
     int kbase;      // first main stage minus the number of min-term stages
@@ -138,7 +146,9 @@ struct Unit {
     int slot;       // tail tile x split + part for a k-part, -1 for a whole tile
 };
 
+template <bool kQ6>
 __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
+    constexpr int kSps = Lay<kQ6>::kStPerSb;
     Unit w;
     int tile;
     if (u < p.full_tiles) {
@@ -151,7 +161,7 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
         const int tail = v / p.split, part = v - tail * p.split;
         tile = p.full_tiles + tail;
         w.slot = v;
-        const int kb0 = 4 * part * p.part_sb, kb1 = min(p.n_main, kb0 + 4 * p.part_sb);
+        const int kb0 = kSps * part * p.part_sb, kb1 = min(p.n_main, kb0 + kSps * p.part_sb);
         const int zst = part == 0 ? p.n_zst : 0;
         w.kbase = kb0 - zst;
         w.n_st = zst + kb1 - kb0;
@@ -170,7 +180,7 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
     uint32_t ph = 0, issued = 0, parity_bits = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit w = unit_of(p, u);
+        const Unit w = unit_of<kQ6>(p, u);
         const int mt = w.mt, nt = w.nt;
         for (int st = 0; st < w.n_st; ++st) {
             if (!cx.wait(p, L::kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
@@ -180,16 +190,18 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
             const uint32_t fb = cx.bar(L::kBarFull + s);
             if (st + w.kbase < 0) {
                 const int j = st / 3, part = st - 3 * j;   // part 0: hi*hi, 1: hi*lo, 2: lo*hi
-                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageB);
+                mbar_arrive_expect_tx(fb, 2 * L::kBox);
                 tma_load_3d(cx.a(s), tm_e, fb, 64 * j, 128 * mt, part == 2 ? 1 : 0);
                 tma_load_3d(cx.b(s), tm_d, fb, 64 * j, 128 * nt, part == 1 ? 1 : 0);
             } else {
                 const int kb = st + w.kbase;
-                const bool sb_last = (kb & 3) == 3;
+                const bool sb_last = (kb + 1) % L::kStPerSb == 0;
                 mbar_arrive_expect_tx(fb, L::kStageA + L::kStageNib + L::kStageHi + L::kStageSc +
                                               (sb_last ? L::kStageD : 0u));
-                tma_load_2d(cx.a(s), tm_x, fb, 64 * kb, 128 * mt);
-                const int64_t rec = static_cast<int64_t>(nt) * p.kc + 2 * kb;
+#pragma unroll
+                for (int i = 0; i < L::kCh / 2; ++i)
+                    tma_load_2d(cx.a(s) + L::kBox * i, tm_x, fb, 64 * (kb * (L::kCh / 2) + i), 128 * mt);
+                const int64_t rec = static_cast<int64_t>(nt) * p.kc + L::kCh * kb;
                 bulk_load(cx.base + L::kOffNib + L::kStageNib * s, p.nib + rec * 128 * 16, L::kStageNib, fb);
                 if constexpr (kQ6) {   // high quant bits, and two scales per row and chunk
                     bulk_load(cx.base + L::kOffHi + L::kStageHi * s, p.q6hi + rec * 128 * 8, L::kStageHi, fb);
@@ -199,7 +211,7 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
                 }
                 if (sb_last)
                     bulk_load(cx.base + L::kOffD + L::kStageD * s,
-                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + (kb >> 2)) * 128, L::kStageD, fb);
+                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + kb / L::kStPerSb) * 128, L::kStageD, fb);
             }
             issued |= 1u << s;
             parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
@@ -226,10 +238,12 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
     uint32_t ph = 0, gph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit w = unit_of(p, u);
+        const Unit w = unit_of<kQ6>(p, u);
         for (int st = 0; st < w.n_st; ++st) {
             const int kb = st + w.kbase;
-            if ((kb >= 0 || st == 0) && !cx.wait(p, L::kBarAccEmpty + g, gph ^ 1u, kSiteMmaAccEmpty)) {
+            // the min-term group is acquired at the unit's first stage, a main
+            // stage's groups (one per two chunks) below
+            if (st == 0 && kb < 0 && !cx.wait(p, L::kBarAccEmpty + g, gph ^ 1u, kSiteMmaAccEmpty)) {
                 ok = false;
                 break;
             }
@@ -244,10 +258,10 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                 break;
             }
             tc_fence_after();
-            const uint64_t ad = sw128_kmajor_desc(cx.a(s));
-            const uint64_t bd = sw128_kmajor_desc(cx.b(s));
-            const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
             if (kb < 0) {
+                const uint64_t ad = sw128_kmajor_desc(cx.a(s));
+                const uint64_t bd = sw128_kmajor_desc(cx.b(s));
+                const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
                     tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
@@ -262,28 +276,40 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                 }
             } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {   // the two 32-k chunks of this stage
-                    const uint32_t tj = tg + 128u * h;
-                    if constexpr (kQ6) {   // bf16: the hi plane, then the lo plane, into one accumulator
-                        const uint64_t bl = sw128_kmajor_desc(cx.b(s) + L::kStageB / 2);
-                        tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMin, 0u);
-                        tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMin, 1u);
-                        tc_mma_f16(tj, ad + 4u * h, bl + 4u * h, kIdescMin, 1u);
-                        tc_mma_f16(tj, ad + 4u * h + 2u, bl + 4u * h + 2u, kIdescMin, 1u);
-                    } else {
-                        tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
-                        tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
+                for (int j = 0; j < L::kCh / 2; ++j) {   // box j: chunks 2j and 2j+1, one group
+                    if (!cx.wait(p, L::kBarAccEmpty + g, gph ^ 1u, kSiteMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_kmajor_desc(cx.a(s) + L::kBox * j);
+                    const uint64_t bd = sw128_kmajor_desc(cx.b(s) + L::kBox * j);
+                    const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t tj = tg + 128u * h;
+                        if constexpr (kQ6) {   // bf16: the hi plane, then the lo plane, into one accumulator
+                            const uint64_t bl = sw128_kmajor_desc(cx.b(s) + L::kStageB / 2);
+                            tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMin, 0u);
+                            tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMin, 1u);
+                            tc_mma_f16(tj, ad + 4u * h, bl + 4u * h, kIdescMin, 1u);
+                            tc_mma_f16(tj, ad + 4u * h + 2u, bl + 4u * h + 2u, kIdescMin, 1u);
+                        } else {
+                            tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
+                            tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
+                        }
+                    }
+                    tc_commit(cx.bar(L::kBarAccFull + g));
+                    if (++g == 2) {
+                        g = 0;
+                        gph ^= 1u;
                     }
                 }
-                tc_commit(cx.bar(L::kBarAccFull + g));
+                if (!ok) break;
                 tc_commit(cx.bar(L::kBarEmpty + s));
                 // the drain reads a stage (its d) only at the end of a super-block;
                 // for every other stage this thread arrives in its place
-                if ((kb & 3) != 3) mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);
-                if (++g == 2) {
-                    g = 0;
-                    gph ^= 1u;
-                }
+                if ((kb + 1) % L::kStPerSb != 0) mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);
             }
             advance<kQ6>(s, ph);
         }
@@ -362,7 +388,7 @@ __device__ __forceinline__ void run_converter(const Ctx<kQ6>& cx, const GemmPara
     uint32_t ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit w = unit_of(p, u);
+        const Unit w = unit_of<kQ6>(p, u);
         for (int st = 0; st < w.n_st; ++st) {
             if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteConvFull)) {
                 ok = false;
@@ -382,9 +408,9 @@ __device__ __forceinline__ void run_converter(const Ctx<kQ6>& cx, const GemmPara
             } else {
                 const uint8_t* nib = cx.sbase + L::kOffNib + L::kStageNib * s;
                 const uint8_t* scs = cx.sbase + L::kOffSc + L::kStageSc * s;
-                uint8_t* brow = cx.sbase + L::kOffB + L::kStageB * s + row_off;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < L::kCh; ++h) {   // chunk h: 64-B half (h & 1) of box h / 2
+                    uint8_t* brow = cx.sbase + L::kOffB + L::kStageB * s + L::kBox * (h >> 1) + row_off;
                     const uint4 w = *reinterpret_cast<const uint4*>(nib + (h * 128 + r) * 16);
                     const __half2 sc2 = __half2half2(__ushort2half_rn(static_cast<unsigned short>(scs[h * 128 + r])));
                     const __half2 nsc2 = __hmul2(sc2, neg1024);   // -1024*sc, exact
@@ -400,7 +426,7 @@ __device__ __forceinline__ void run_converter(const Ctx<kQ6>& cx, const GemmPara
                             const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&pr), sc2, nsc2);
                             o[jj] = *reinterpret_cast<const uint32_t*>(&v);
                         }
-                        const uint32_t g = static_cast<uint32_t>(4 * h + i);
+                        const uint32_t g = static_cast<uint32_t>(4 * (h & 1) + i);
                         *reinterpret_cast<uint4*>(brow + ((g ^ rx) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
@@ -546,7 +572,7 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
     uint32_t ph = 0, gph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit w = unit_of(p, u);
+        const Unit w = unit_of<kQ6>(p, u);
         const int mt = w.mt, nt = w.nt;
         const int64_t t = static_cast<int64_t>(mt) * 128 + row;
         const int col0 = nt * 128 + 64 * ch;
@@ -557,12 +583,12 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
             P[j] = 0.0f;
         }
         // d_a straight from global memory (this thread's token, two chunks per
-        // stage), loaded one main stage ahead so that its latency is hidden
-        const int kb_end = w.kbase + w.n_st;
+        // accumulator group), loaded one group ahead so that its latency is hidden
+        const int c_end = L::kCh * (w.kbase + w.n_st);
         const float* dap = p.da + static_cast<int64_t>(mt) * p.kc * 128 + row;   // + 128 * chunk
         float da_n0 = 0.0f, da_n1 = 0.0f;
-        if (max(w.kbase, 0) < kb_end) {
-            const int c0 = 2 * max(w.kbase, 0);
+        if (L::kCh * max(w.kbase, 0) < c_end) {
+            const int c0 = L::kCh * max(w.kbase, 0);
             da_n0 = __ldg(dap + 128 * c0);
             da_n1 = __ldg(dap + 128 * (c0 + 1));
         }
@@ -591,46 +617,51 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
                     gph ^= 1u;
                 }
             } else if (kb >= 0) {
-                const float da0 = da_n0, da1 = da_n1;
-                if (kb + 1 < kb_end) {
-                    da_n0 = __ldg(dap + 128 * (2 * kb + 2));
-                    da_n1 = __ldg(dap + 128 * (2 * kb + 3));
-                }
-                if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiAccFull)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tg = cx.tmem + lane_off + 256u * static_cast<uint32_t>(g) + 64u * ch;
+#pragma unroll 1
+                for (int j = 0; j < L::kCh / 2; ++j) {   // one accumulator group per two chunks
+                    const int c = L::kCh * kb + 2 * j;    // its first chunk
+                    const float da0 = da_n0, da1 = da_n1;
+                    if (c + 2 < c_end) {
+                        da_n0 = __ldg(dap + 128 * (c + 2));
+                        da_n1 = __ldg(dap + 128 * (c + 3));
+                    }
+                    if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiAccFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tg = cx.tmem + lane_off + 256u * static_cast<uint32_t>(g) + 64u * ch;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float da = h ? da1 : da0;
+                    for (int h = 0; h < 2; ++h) {
+                        const float da = h ? da1 : da0;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t J[16];
-                        tmem_ld16(tg + 128u * h + 16u * q, J);
-                        tmem_wait_ld();
-                        if (h == 1 && q == 3) {   // both accumulators read: the group goes back to the MMA
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + g));
-                        }
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t J[16];
+                            tmem_ld16(tg + 128u * h + 16u * q, J);
+                            tmem_wait_ld();
+                            if (h == 1 && q == 3) {   // both accumulators read: the group goes back to the MMA
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + g));
+                            }
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2)
-                            ffma2(P[16 * q + j], P[16 * q + j + 1], da, da, __uint_as_float(J[j]),
-                                  __uint_as_float(J[j + 1]));
-                        if (kDump && t < p.m) {
+                            for (int jj = 0; jj < 16; jj += 2)
+                                ffma2(P[16 * q + jj], P[16 * q + jj + 1], da, da, __uint_as_float(J[jj]),
+                                      __uint_as_float(J[jj + 1]));
+                            if (kDump && t < p.m) {
 #pragma unroll 4
-                            for (int j = 0; j < 16; ++j)
-                                p.dbg[(t * p.n + col0 + 16 * q + j) * p.kc + 2 * kb + h] = __uint_as_float(J[j]);
+                                for (int jj = 0; jj < 16; ++jj)
+                                    p.dbg[(t * p.n + col0 + 16 * q + jj) * p.kc + c + h] = __uint_as_float(J[jj]);
+                            }
                         }
                     }
+                    if (++g == 2) {
+                        g = 0;
+                        gph ^= 1u;
+                    }
                 }
-                if (++g == 2) {
-                    g = 0;
-                    gph ^= 1u;
-                }
-                if ((kb & 3) == 3) {   // super-block done: Y += d * P, d from this stage
+                if (!ok) break;
+                if ((kb + 1) % L::kStPerSb == 0) {   // super-block done: Y += d * P, d from this stage
                     if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteEpiFull)) {
                         ok = false;
                         break;

@@ -27,6 +27,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// 32-k chunks per main stage of the tensor-core GEMM: 4 (128 k) for Q4_K,
+// 2 (64 k) for Q6_K, whose stages carry two bf16 weight planes.
+__host__ __device__ constexpr int gemm_chunks_per_stage(bool q6) { return q6 ? 2 : 4; }
+
 struct GemmParams {
     const uint8_t* nib;     // packed quants  [nt][kc][128][16 B]
     const uint8_t* sc;      // packed scales  [nt][kc][128]
