@@ -57,7 +57,7 @@ constexpr int kThreads = 512;
 // quants, sc and d.  Q6_K: four stages of 64 k (the B tile has two bf16
 // planes, hi and lo) plus the high quant bits.  A and B tiles are made of
 // 16 KB boxes of 128 rows x 64 k (128-B rows, 128-B swizzle), one per two
-// chunks.  A min-term stage uses the first box of A and of B.
+// chunks.  A min-term stage uses as many boxes of A and B, each 64 deep.
 template <bool kQ6>
 struct Lay {
     static constexpr int kCh = gemm_chunks_per_stage(kQ6);     // 32-k chunks per main stage
@@ -189,10 +189,16 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
             }
             const uint32_t fb = cx.bar(L::kBarFull + s);
             if (st + w.kbase < 0) {
+                // min-term stage: depth block j (32 kCh chunks of the rank-kc
+                // product, one box of 64 per two) of hi/lo part `part`
                 const int j = st / 3, part = st - 3 * j;   // part 0: hi*hi, 1: hi*lo, 2: lo*hi
-                mbar_arrive_expect_tx(fb, 2 * L::kBox);
-                tma_load_3d(cx.a(s), tm_e, fb, 64 * j, 128 * mt, part == 2 ? 1 : 0);
-                tma_load_3d(cx.b(s), tm_d, fb, 64 * j, 128 * nt, part == 1 ? 1 : 0);
+                mbar_arrive_expect_tx(fb, 2 * L::kBox * (L::kCh / 2));
+#pragma unroll
+                for (int i = 0; i < L::kCh / 2; ++i) {   // boxes wholly past kc read zeros
+                    const int x = 32 * L::kCh * j + 64 * i;
+                    tma_load_3d(cx.a(s) + L::kBox * i, tm_e, fb, x, 128 * mt, part == 2 ? 1 : 0);
+                    tma_load_3d(cx.b(s) + L::kBox * i, tm_d, fb, x, 128 * nt, part == 1 ? 1 : 0);
+                }
             } else {
                 const int kb = st + w.kbase;
                 const bool sb_last = (kb + 1) % L::kStPerSb == 0;
@@ -259,12 +265,15 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
             }
             tc_fence_after();
             if (kb < 0) {
-                const uint64_t ad = sw128_kmajor_desc(cx.a(s));
-                const uint64_t bd = sw128_kmajor_desc(cx.b(s));
                 const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
-                    tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
+                for (int i = 0; i < L::kCh / 2; ++i) {
+                    const uint64_t ad = sw128_kmajor_desc(cx.a(s) + L::kBox * i);
+                    const uint64_t bd = sw128_kmajor_desc(cx.b(s) + L::kBox * i);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
+                        tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | i | kk) != 0 ? 1u : 0u);
+                }
                 tc_commit(cx.bar(L::kBarEmpty + s));
                 mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);   // the drain reads nothing of this stage
                 if (kb == -1) {   // Z complete: the group goes to the drain
