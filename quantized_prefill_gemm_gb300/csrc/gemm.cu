@@ -640,28 +640,32 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
                     }
                     tc_fence_after();
                     const uint32_t tg = cx.tmem + lane_off + 256u * static_cast<uint32_t>(g) + 64u * ch;
+                    // eight 16-column pieces (chunk pc / 4, columns 16 (pc % 4)): the
+                    // next piece's load is in flight while this one is folded
+                    uint32_t Ja[16], Jb[16];
+                    tmem_ld16(tg, Ja);
+                    tmem_wait_ld16(Ja);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float da = h ? da1 : da0;
+                    for (int pc = 0; pc < 8; ++pc) {
+                        uint32_t (&Jc)[16] = (pc & 1) ? Jb : Ja;
+                        uint32_t (&Jn)[16] = (pc & 1) ? Ja : Jb;
+                        if (pc + 1 < 8) tmem_ld16(tg + 128u * ((pc + 1) >> 2) + 16u * ((pc + 1) & 3), Jn);
+                        const float da = pc < 4 ? da0 : da1;
+                        const int q = pc & 3;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t J[16];
-                            tmem_ld16(tg + 128u * h + 16u * q, J);
-                            tmem_wait_ld();
-                            if (h == 1 && q == 3) {   // both accumulators read: the group goes back to the MMA
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + g));
-                            }
-#pragma unroll
-                            for (int jj = 0; jj < 16; jj += 2)
-                                ffma2(P[16 * q + jj], P[16 * q + jj + 1], da, da, __uint_as_float(J[jj]),
-                                      __uint_as_float(J[jj + 1]));
-                            if (kDump && t < p.m) {
+                        for (int jj = 0; jj < 16; jj += 2)
+                            ffma2_ordered(P[16 * q + jj], P[16 * q + jj + 1], da, da, __uint_as_float(Jc[jj]),
+                                          __uint_as_float(Jc[jj + 1]));
+                        if (kDump && t < p.m) {
 #pragma unroll 4
-                                for (int jj = 0; jj < 16; ++jj)
-                                    p.dbg[(t * p.n + col0 + 16 * q + jj) * p.kc + c + h] = __uint_as_float(J[jj]);
-                            }
+                            for (int jj = 0; jj < 16; ++jj)
+                                p.dbg[(t * p.n + col0 + 16 * q + jj) * p.kc + c + (pc >> 2)] = __uint_as_float(Jc[jj]);
+                        }
+                        if (pc + 1 < 8) tmem_wait_ld16(Jn);
+                        if (pc == 6) {   // both accumulators read: the group goes back to the MMA
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(cx.bar(L::kBarAccEmpty + g));
                         }
                     }
                     if (++g == 2) {

@@ -247,6 +247,28 @@ __device__ __forceinline__ void ffma2(float& c0, float& c1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// The same as a volatile asm: kept in program order relative to the TMEM
+// loads and waits around it (the drain folds one piece while the next loads).
+__device__ __forceinline__ void ffma2_ordered(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+    asm volatile("{\n\t.reg .b64 ra, rb, rc;\n\t"
+                 "mov.b64 ra, {%2, %3};\n\t"
+                 "mov.b64 rb, {%4, %5};\n\t"
+                 "mov.b64 rc, {%0, %1};\n\t"
+                 "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+                 "mov.b64 {%0, %1}, rc;\n\t}"
+                 : "+f"(c0), "+f"(c1)
+                 : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// tcgen05.wait::ld that also names the 16 registers of the load it completes,
+// so that no use of them can be placed before it
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
+                 :
+                 : "memory");
+}
+
 // Warpgroup register re-split (all four warps of a warpgroup execute the same
 // one).  .inc waits until other warpgroups' .dec have returned registers, so
 // the shares must add up to at most the CTA's launch allocation.
