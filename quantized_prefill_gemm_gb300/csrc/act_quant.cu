@@ -7,11 +7,11 @@
 // qa = clamp(rint_half_even(RN32(x*inv)), -127, 127), d_a = RN16(d);
 // blocks with amax < 2^-120 are zero blocks.
 //
-// One thread per block (q8_rows_kernel, act_quant_kernel): its eight 16-B
-// loads are in flight together and amax and ssum need no shuffles; a warp
-// takes 32 consecutive blocks of one token (4 KB of contiguous fp32).  Small
-// batches of the public q8 form, and the q8-to-operand conversion, use an
-// 8-lane group per block.  HBM-bound: 4 B
+// The public q8 form (q8_rows_kernel): one thread per block, its eight 16-B
+// loads in flight together, amax and ssum without shuffles; a warp takes 32
+// consecutive blocks of one token (4 KB of contiguous fp32).  Its small
+// batches, the GEMM operand form (act_quant_kernel) and the q8-to-operand
+// conversion use an 8-lane group per block.  HBM-bound: 4 B
 // read per element, 1 B (public q8) or 2 B (GEMM operand) written per element
 // plus a few bytes per block.
 #include <cuda_bf16.h>
@@ -195,10 +195,14 @@ __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64
     }
 }
 
-// GEMM operand form (see q4k_layout.h; codes as fp16, or bf16 with kBf16) from fp32 activations.  One thread
-// per 32-k block: its eight 16-B loads are in flight together, amax and ssum
-// need no shuffles, and a warp covers 32 consecutive blocks of one token
-// (4 KB of contiguous fp32 in, 2 KB of fp16 and 64 + 64 B of d_a*ssum out).
+// GEMM operand form (see q4k_layout.h; codes as fp16, or bf16 with kBf16)
+// from fp32 activations.  A warp takes 8 consecutive 32-k blocks of one token
+// (1 KB of fp32; k is a multiple of 256, so the blocks of a token come in
+// whole eights), and an 8-lane group one block per 16-B load: each load
+// instruction reads 512 contiguous bytes, each code store writes 256, and the
+// lane's two loads are in flight together.  The input is read once, so it is
+// loaded with the evict-first hint and leaves L2 to the operand the GEMM
+// reads next.
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float* __restrict__ x, int64_t m,
                                                                      int64_t mp, int64_t k, int64_t ldx,
@@ -207,28 +211,25 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float
                                                                      __nv_bfloat16* __restrict__ e) {
     griddep_launch_dependents();   // programmatic dependent launch (see q8_rows_kernel)
     griddep_wait();
-    const int64_t kc = k / 32, kg = (kc + 31) / 32;   // 32-block groups per token
+    const int64_t kc = k / 32, units = kc / 8;
     const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t t = wid / kg, c = (wid % kg) * 32 + lane;
-    if (t >= mp || c >= kc) return;
-    float* da_slot = dat + ((t >> 7) * kc + c) * 128 + (t & 127);
+    const int64_t t = wid / units, c0 = (wid % units) * 8;
+    if (t >= mp) return;
+    const int j = lane & 7, b = lane >> 3;   // float4 j of blocks c0 + b and c0 + 4 + b
     if (t >= m) {   // padding token of the last 128-token tile: scale 0
-        *da_slot = 0.0f;
+        if (j == 0) {
+            dat[((t >> 7) * kc + c0 + b) * 128 + (t & 127)] = 0.0f;
+            dat[((t >> 7) * kc + c0 + 4 + b) * 128 + (t & 127)] = 0.0f;
+        }
         return;
     }
-    const BlockQ8 b = quantize_block(x + t * ldx + c * 32);
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = code_pair<kBf16>(b.q[2 * i], b.q[2 * i + 1]);
-    uint4* dst = reinterpret_cast<uint4*>(xq + t * k + c * 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    *da_slot = __half2float(b.da);
-    __nv_bfloat16 hi, lo;
-    split_e(b.da, b.ssum, hi, lo);
-    e[t * kc + c] = hi;
-    e[(m + t) * kc + c] = lo;
+    const float4* src = reinterpret_cast<const float4*>(x + t * ldx + c0 * 32);
+    const float4 v0 = __ldcs(src + lane), v1 = __ldcs(src + 32 + lane);
+    const LaneQ8 r0 = quantize_lane(v0);
+    const LaneQ8 r1 = quantize_lane(v1);
+    write_operand<kBf16>(t, c0 + b, j, m, k, kc, r0.q, r0.da, r0.ssum, xq, dat, e);
+    write_operand<kBf16>(t, c0 + 4 + b, j, m, k, kc, r1.q, r1.da, r1.ssum, xq, dat, e);
 }
 
 // GEMM operand form from the public q8 SoA ([m][ldq] int8, da, ssum [m][kc]).
@@ -283,7 +284,7 @@ cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ld
                                 cudaStream_t s) {
     const ActLayout L(m, k);
     const int64_t mp = align_up(m, kTileM);
-    const int64_t threads = mp * ((k / 32 + 31) / 32) * 32;   // a warp per 32 blocks of a token
+    const int64_t threads = mp * (k / 32) * 4;   // a warp per 8 blocks of a token
     if (threads == 0) return cudaSuccess;
     uint8_t* b = static_cast<uint8_t*>(ws);
     uint16_t* xq = reinterpret_cast<uint16_t*>(b + L.xq);
