@@ -356,17 +356,17 @@ __device__ __forceinline__ void convert_q6(const Ctx<kQ6>& cx, int s, int r, uin
         const uint32_t hw[4] = {wh.x, wh.x >> 2, wh.y, wh.y >> 2};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {   // 8-k group i of chunk h
-            // q (0..63) per byte: low nibble, high bits, and u ^ 32 undone
-            uint32_t l0, l1, h0, h1;
-            unpack_group(lw[i], l0, l1);
-            unpack_group(hw[i] & 0x33333333u, h0, h1);
-            const uint32_t q[2] = {(l0 | (h0 << 4)) ^ 0x20202020u, (l1 | (h1 << 4)) ^ 0x20202020u};
             const __nv_bfloat162 sc = i < 2 ? sc0 : sc1;
             uint32_t ohi[4], olo[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                // bf16 pair 128 + q (byte q under the exponent byte 0x43), minus 160: v = q - 32, exact
-                const uint32_t raw = __byte_perm(q[jj >> 1], 0x43434343u, (jj & 1) ? 0x4342u : 0x4140u);
+                // the pair k = 2jj, 2jj+1 straight from the packed words: the low
+                // nibbles sit at bits 4jj and 16+4jj, the 2-bit high fields at the
+                // same places of the shifted high-bit word.  bf16(128 + q) is the
+                // pattern 0x4300 | q; the stored field is u = q ^ 32, so bit 5 is
+                // flipped with the exponent bits in one step.  Minus 160: v = q - 32, exact.
+                const uint32_t hf = jj == 0 ? (hw[i] << 4) : (hw[i] >> (4 * jj - 4));
+                const uint32_t raw = ((lw[i] >> (4 * jj)) & 0x000F000Fu) | ((hf & 0x00300030u) ^ 0x43204320u);
                 const __nv_bfloat162 v = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&raw), m160);
                 const __nv_bfloat162 h2 = __hmul2(v, sc);                 // hi = RN_bf16(sc * v)
                 const __nv_bfloat162 l2 = __hfma2(v, sc, __hneg2(h2));    // lo = sc * v - hi, exact
