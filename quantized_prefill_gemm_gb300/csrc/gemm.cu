@@ -100,9 +100,10 @@ static_assert(128 * kRegsCtl + 128 * kRegsConv + 256 * kRegsDrain <= 65536, "reg
 constexpr uint32_t kIdescMain = idesc_kind_f16(128, 128, false);   // fp16 x fp16 -> fp32
 constexpr uint32_t kIdescMin = idesc_kind_f16(128, 128, true);     // bf16 x bf16 -> fp32
 
-// wait sites recorded in the error word
+// wait sites recorded in the error word (numbers kept stable; 2 is no longer
+// used: the running Y left TMEM, and with it the MMA's wait for a free Y)
 enum : unsigned {
-    kSiteProdEmpty = 1, kSiteMmaYEmpty, kSiteMmaFull, kSiteMmaConv, kSiteMmaAccEmpty,
+    kSiteProdEmpty = 1, kSiteUnused2, kSiteMmaFull, kSiteMmaConv, kSiteMmaAccEmpty,
     kSiteConvFull, kSiteEpiFull, kSiteEpiAccFull, kSiteEpiZ
 };
 
