@@ -23,11 +23,11 @@
 // output tile at a time, k in stages of 128 for Q4_K and 64 for Q6_K (four or
 // two chunks of 32):
 //   warp 0        TMA producer: activation tile (fp16, 128-B swizzle), packed
-//                 quants, sc, da, d; for the min-term stages the bf16 E and
-//                 -(dmin*m) tiles
+//                 quants, sc, and d at super-block ends; for the min-term
+//                 stages the bf16 E and -(dmin*m) tiles
 //   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk, two chunks into
 //                 the two accumulators of one TMEM group, one commit for both;
-//                 4 bf16 MMAs per min-term stage into a group's first one
+//                 4 bf16 MMAs per 64 of min-term depth into a group's first one
 //   warps 2-3     no role (they complete the first warpgroup)
 //   warps 4-7     converters: 4-bit quants -> fp16 sc*q written in the
 //                 128-B-swizzled K-major layout the MMA reads
@@ -233,11 +233,12 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
 
 // ----------------------------------------------------------- MMA issuer --
 // TMEM holds four 128-column accumulators in two groups (group g: columns
-// 256 g .. 256 g + 255).  One group use is one 64-k main stage (chunk h of
-// the stage accumulates into column 256 g + 128 h) or, at the start of a unit
-// with min-term stages, all of its min-term stages (Z accumulates into the
-// group's first accumulator).  One commit hands a whole group to the drain,
-// and the drain hands it back with one arrival per warp.
+// 256 g .. 256 g + 255).  One group use is one 16 KB box of a main stage, two
+// chunks of 32 k (chunk h of the box accumulates into column 256 g + 128 h),
+// or, at the start of a unit with min-term stages, all of its min-term stages
+// (Z accumulates into the group's first accumulator).  One commit hands a
+// whole group to the drain, and the drain hands it back with one arrival per
+// warp.
 template <bool kQ6>
 __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p) {
     using L = Lay<kQ6>;
