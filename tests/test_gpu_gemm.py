@@ -167,11 +167,11 @@ def test_bounded_wait_selftest(q4k):
 
 
 def test_k_split_tail_and_workspace_reuse(q4k):
-    """Tiles left over after the last full wave are split along k into parts
-    whose partial tiles are added by the part that finishes last; the arrival
-    counters live in the workspace and are left at zero.  16 tiles with 8
-    super-blocks each split 8 ways on a 152-SM part: every output against the
-    oracle, three calls on one workspace giving the same bits."""
+    """Tiles left over after the last full wave are split along k into parts of
+    whole super-blocks; each part stores its partial tile in the workspace and
+    a fixup kernel adds them in part order.  16 tiles with 8 super-blocks each
+    split 8 ways on a 152-SM part: every output against the oracle, three
+    calls on one workspace giving the same bits."""
     m, n, k = 256, 1024, 2048
     blocks, x = make_case(n, k, m, "outlier", seed=91)
     packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
@@ -181,3 +181,23 @@ def test_k_split_tail_and_workspace_reuse(q4k):
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
     want, scale = oracle_rows(blocks, x, np.arange(m))
     assert_close(ys[0].cpu().double().numpy(), want, scale, "f32", "k-split tail")
+
+
+def test_long_k_min_term_boxes_and_exact_chunks(q4k):
+    """K = 14336 (448 chunks): 112 main stages of 128 k and 12 min-term stages,
+    whose last depth block holds one box partly and one wholly past kc (read as
+    zeros); 150 tokens leave the token tile ragged.  Every output against the
+    oracle, and every per-chunk integer exact."""
+    m, n, k = 150, 256, 14336
+    blocks, x = make_case(n, k, m, "outlier", seed=123)
+    y = _run(q4k, blocks, x, n, k, "f32")
+    want, scale = oracle_rows(blocks, x, np.arange(m))
+    assert_close(y, want, scale, "f32", "long k")
+    packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+    ws = q4k.q4k_act_quantize(to_dev(x))
+    _, acc = q4k.q4k_gemm_debug_chunk_acc(packed, n, k, ws, m)
+    torch.cuda.synchronize()
+    fields = q4k_blocks.decode(blocks)
+    qa, _, _ = oq8.quantize_rows(x)
+    dots = ogemm.chunk_dots(fields, qa) * fields["sc"].astype(np.int64)[None, :, :]
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), dots)
