@@ -94,6 +94,48 @@ def gemm_launches(m, n, k, sms):
     return 3 if split else 2
 
 
+L2_BYTES = 129 * 10**6          # GB300 L2
+FLUSH_BYTES = 512 * 2**20       # written between timed steps when a step's inputs fit in L2
+
+
+def step_footprint(tokens, mats, out, wbytes_per_256):
+    """Algorithmic bytes of one step: packed weights, fp32 activations in, Y out."""
+    w = sum(n * k for n, k in mats) * wbytes_per_256 / 256
+    x = sum(tokens * k * 4 for _, k in mats)
+    y = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
+    return w, x, y
+
+
+def time_steps(torch, stream, steps, body, flush):
+    """Device time of `steps` calls of body(s) in ms.  Without a flush buffer
+    the steps run back to back between two events; with one, the buffer is
+    overwritten before each step (outside its events), so that no input of the
+    step is served from L2, and the steps' own event times are summed."""
+    if flush is None:
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for s in range(steps):
+            body(s)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(stop)
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        marks[s][0].record(stream)
+        body(s)
+        marks[s][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in marks)
+
+
+def hbm_view(peaks, src, nbytes, ms_step, what):
+    achieved = nbytes / (ms_step * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    return {"bytes_per_step": nbytes, "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{src} HBM copy bandwidth", "what": what}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -269,18 +311,15 @@ def main():
         dist.barrier()
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in mats]
           for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wb, xb, yb = step_footprint(tokens, mats, out, 210 if q6 else 144)
+    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if wb + xb + yb < 2 * L2_BYTES else None)
     clocks = ClockSampler(local)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("timed")
-    start.record(stream)
-    for s in range(args.steps):
-        step(ev[s])
-    stop.record(stream)
+    step_ms = time_steps(torch, stream, args.steps, lambda s: step(ev[s]), flush)
     torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize()
     clk = clocks.stop()
-    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
+    total_ms = max_over_ranks(step_ms, dist, dev)
     ms_step = total_ms / args.steps
     gemm_ms = sum(a.elapsed_time(b) for s in ev for (a, b) in s)
     flops_step = sum(2.0 * tokens * n * k for n, k in mats)
@@ -315,9 +354,16 @@ def main():
                       else "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers"),
             "data": "synthetic (seeded random {} weights and activations)".format("Q6_K" if q6 else "Q4_K"),
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
-                       "l2": "inputs larger than L2 (whole step touches >18 GB)", "parallelism": f"replicas x{world}"},
+                       "l2": (f"L2 flushed before each timed step ({FLUSH_BYTES >> 20} MB written outside the step's "
+                              f"events): a step touches only {(wb + xb + yb) / 1e6:.0f} MB" if flush is not None else
+                              f"inputs larger than L2 (a step touches {(wb + xb + yb) / 1e9:.2f} GB)"),
+                       "parallelism": f"replicas x{world}"},
             "effective_tops": eff_tops, "gemm_ms_per_step": gemm_ms / args.steps,
-            "roofline": roofline, "clocks": clk,
+            "roofline": roofline,
+            "hbm": hbm_view(peaks, src, wb + xb + yb, ms_step,
+                            "algorithmic bytes per step (packed weights at {} B/256, fp32 X, Y at its dtype) / "
+                            "step time: distance from the HBM limit of a tensor-bound path".format(210 if q6 else 144)),
+            "clocks": clk,
             "gpu_launches": sum(gemm_launches(tokens, n, k, sms) for n, k in mats) * args.steps}
     if e2e is not None:
         line["e2e"] = e2e
@@ -364,16 +410,14 @@ def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
     if dist:
         dist.barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # algorithmic bytes: pair and down weights, fp32 x, bf16 y (h stays in the operand form, 2.25 B/element)
+    fbytes = (2 * nf * k + 4096 * nf) * 144 / 256 + tokens * k * 4 + tokens * 4096 * 2
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if fbytes < 2 * L2_BYTES else None
     clocks = ClockSampler(local)
     torch.cuda.synchronize()
-    start.record(stream)
-    for s_ in range(args.steps):
-        step(evs[s_])
-    stop.record(stream)
-    torch.cuda.synchronize()
+    step_ms = time_steps(torch, stream, args.steps, lambda s_: step(evs[s_]), flush)
     clk = clocks.stop()
-    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
+    total_ms = max_over_ranks(step_ms, dist, dev)
     err = q4k.q4k_device_error_word()
     if err:
         raise RuntimeError(f"device error word 0x{err:x}")
@@ -389,14 +433,22 @@ def run_ffn_swiglu(args, q4k, inputs, torch, dev, dist, world, rank, local):
             "dtype": "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers",
             "data": "synthetic (seeded random Q4_K weights and activations)",
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": 2,
-                       "l2": "weights 76 MB + 25 MB, activations 34 MB in / 45 MB between the GEMMs",
+                       "l2": ((f"L2 flushed before each timed step ({FLUSH_BYTES >> 20} MB written outside the "
+                               "step's events): ") if flush is not None else "") +
+                             "weights 76 MB + 25 MB, activations 34 MB in / 45 MB between the GEMMs",
                        "parallelism": f"replicas x{world}"},
             "effective_tops": world * flops_step / (ms_step * 1e-3) / 1e12, "gemm_ms_per_step": gemm_ms,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None, "kernel": "q4k_gemm_kernel",
                          "peak_source": f"{src} bf16 dense, sustained",
                          "per_launch": "2*M*N*K of the pair and down GEMMs / their CUDA-event time per step"},
-            "clocks": clk, "gpu_launches": 3 * args.steps}
+            "hbm": hbm_view(peaks, src, fbytes, ms_step,
+                            "algorithmic bytes per step (packed weights at 144 B/256, fp32 x, bf16 y) / step time"),
+            "clocks": clk,
+            "gpu_launches": (1 + (gemm_launches(tokens, 2 * nf, k, min(torch.cuda.get_device_properties(dev)
+                                                                        .multi_processor_count, 160)) - 1)
+                             + (gemm_launches(tokens, 4096, nf, min(torch.cuda.get_device_properties(dev)
+                                                                    .multi_processor_count, 160)) - 1)) * args.steps}
     if not args.no_e2e and rank == 0:
         hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
         hx.copy_(x)
@@ -569,16 +621,14 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
     if dist:
         dist.barrier()
 
+    wbytes_total = sum(n * k * (210 if q6 else 144) / 256 for n, k in mats)
+    # weights that fit in L2 would be served from it by the next replay: flush between replays then
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if wbytes_total < 2 * L2_BYTES else None
+
     def timed(g, reps):   # replays run on the current stream; the events bracket them there
         cur = torch.cuda.current_stream()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        a.record(cur)
-        for _ in range(reps):
-            g.replay()
-        b.record(cur)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+        return time_steps(torch, cur, reps, lambda s: g.replay(), flush) / reps
 
     clocks = ClockSampler(local)
     torch.cuda.nvtx.range_push("timed")
@@ -610,7 +660,8 @@ def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs
             "data": "synthetic (seeded random {} weights and activations)".format("Q6_K" if q6 else "Q4_K"),
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
                        "l2": f"{weights_gb:.2f} GB of weights per step" + (
-                           " (larger than L2)" if weights_gb > 0.2 else " (L2-resident between replays)"),
+                           " (larger than L2)" if flush is None else
+                           f" (L2 flushed before each timed replay, {FLUSH_BYTES >> 20} MB written outside its events)"),
                        "parallelism": f"replicas x{world}"},
             "effective_tops": world * flops_step / (ms_step * 1e-3) / 1e12,
             "products_ms_per_step": ms_products, "roofline": roofline, "clocks": clk,
