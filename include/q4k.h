@@ -207,7 +207,7 @@ q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t
                                      void* h_ws, size_t h_ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
- * Q6_K weights (decode sizes).  The series moves on from Q4_K to a Q6_K line
+ * Q6_K weights.  The series moves on from Q4_K to a Q6_K line
  * ("34 · r31 — q-major sda scale-read repack", §5 Results, post-hoc notes);
  * the pages give no layout for it.  Blocks follow the public GGUF Q6_K
  * format: 256 weights in 210 bytes (ql[128] low 4 bits, qh[64] high 2 bits,
@@ -216,15 +216,16 @@ q4k_status q4k_gemm_swiglu_quantized(const void* packed_pair, int64_t n, int64_t
  * q6k_pack_weights  blocks [n][k/256] x 210 B (device) -> packed
  *            (q6k_packed_bytes(n, k) bytes, 256-byte aligned).
  * q6k_gemm   as q4k_gemm (same arguments, activation forms and accuracy
- *            contract) for 1 <= m <= Q4K_SMALL_M tokens: per 32-k block the
- *            exact integer sum_s sc_s * sum (q - 32) * qa (two 16-weight
- *            sub-blocks), then d_a * d times it.  With f32 input and
- *            m <= Q4K_FUSED_QUANT_M the kernel quantizes the activations
- *            itself (workspace unused); for larger m the q8 SoA goes to the
- *            start of `workspace` (q4k_gemm_workspace_bytes(m, n, k, act)).
- *            Larger m (and activations too large for the kernel's shared
- *            memory: m x k bytes plus scales, at most ~200 KB) return
- *            Q4K_ERR_SHAPE: the tensor-core path covers Q4_K only.
+ *            contract): per 32-k block the exact integer
+ *            sum_s sc_s * sum (q - 32) * qa (two 16-weight sub-blocks), then
+ *            d_a * d times it.  For 1 <= m <= Q4K_SMALL_M tokens whose
+ *            activations fit the small-M kernel's shared memory (m x k bytes
+ *            plus scales, at most ~200 KB) it runs on the CUDA cores: with
+ *            f32 input and m <= Q4K_FUSED_QUANT_M the kernel quantizes the
+ *            activations itself (workspace unused), otherwise the q8 SoA goes
+ *            to the start of `workspace`.  Larger m take the tensor-core
+ *            GEMM, which quantizes into `workspace` as q4k_gemm does.
+ *            workspace_bytes >= q4k_gemm_workspace_bytes(m, n, k, act).
  * n % 128 == 0, k % 256 == 0.
  * ------------------------------------------------------------------------ */
 size_t q6k_packed_bytes(int64_t n, int64_t k);
@@ -286,8 +287,9 @@ q4k_status q4k_gemm_static_workspace(const void* packed_w, int64_t n, int64_t k,
  * q6k_gemm_debug_chunk_acc  the same for Q6_K weights on the tensor-core
  *                        path: J[t][o][c] = sum_s sc_s * sum (q - 32) * qa
  *                        over the chunk's two sub-blocks; workspace holds the
- *                        bf16 operand form (from q6k_gemm's own quantization,
- *                        i.e. a prior q6k_gemm call with m > 16 on it).
+ *                        operand form (from q6k_gemm's own quantization, i.e.
+ *                        a prior q6k_gemm call with m > 16 on it, or
+ *                        q4k_act_quantize).
  * ------------------------------------------------------------------------ */
 unsigned int q4k_device_error_word(int reset);
 q4k_status q4k_device_status(int reset);

@@ -136,8 +136,8 @@ q4k_status check_output(const void* y, int64_t m, int64_t n, int out, int64_t ld
 
 // h_ws (gate/up pair weights only): instead of Y, write the down projection's
 // operand of SiLU(gate)*up, ActLayout(m, n / 2), there; y, out and ldy are then
-// unused.  The caller has checked h_ws.  q6: Q6_K weights (Q6Layout) and a
-// bf16 activation operand in ws.
+// unused.  The caller has checked h_ws.  q6: Q6_K weights (Q6Layout); the
+// activation operand in ws has the same fp16 form as for Q4_K.
 q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t ws_bytes, int64_t m, void* y,
                     int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream, bool q6 = false) {
     q4k_status st = check_gemm_shape(n, k, m);
@@ -157,7 +157,7 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     uint8_t* ab = static_cast<uint8_t*>(ws);
     const int64_t kc = k / 32;
     CUtensorMap tm_x, tm_e, tm_d;
-    if ((st = encode_map(&tm_x, q6 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ab + A.xq, k,
+    if ((st = encode_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ab + A.xq, k,
                          m, 1)) != Q4K_OK)
         return st;
     if (q6) {   // no min term: the min-term maps are not used
@@ -380,7 +380,7 @@ q4k_status q4k_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, v
     if (workspace_bytes < q4k_act_workspace_bytes(m, k)) return Q4K_ERR_WORKSPACE;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != Q4K_OK) return st;
-    return from_cuda(launch_act_quantize(x, m, k, ldx, workspace, false, stream));
+    return from_cuda(launch_act_quantize(x, m, k, ldx, workspace, stream));
 }
 
 q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16_t* ssum, int64_t m, int64_t k,
@@ -394,7 +394,7 @@ q4k_status q4k_act_from_q8(const int8_t* q8, const uint16_t* da_f16, const int16
     DeviceInfo* dev = nullptr;
     q4k_status st = device_info(&dev);
     if (st != Q4K_OK) return st;
-    return from_cuda(launch_act_from_q8(q8, da_f16, ssum, m, k, ldq, workspace, false, stream));
+    return from_cuda(launch_act_from_q8(q8, da_f16, ssum, m, k, ldq, workspace, stream));
 }
 
 q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k, void* workspace,
@@ -522,14 +522,14 @@ q4k_status q6k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
         if (act == Q4K_ACT_F32) {
             const float* xf = static_cast<const float*>(x_or_q8);
             if ((st = check_act_f32(xf, m, k, ldx)) != Q4K_OK) return st;
-            st = from_cuda(launch_act_quantize(xf, m, k, ldx, workspace, true, stream));
+            st = from_cuda(launch_act_quantize(xf, m, k, ldx, workspace, stream));
         } else {
             const int8_t* q8 = static_cast<const int8_t*>(x_or_q8);
             if (!q8 || !da_f16 || !ssum) return Q4K_ERR_INVALID_ARG;
             if (ldx < k) return Q4K_ERR_SHAPE;
             if (!aligned(q8, 4) || ldx % 4 || !aligned(da_f16, 2) || !aligned(ssum, 2)) return Q4K_ERR_ALIGNMENT;
             st = from_cuda(launch_act_from_q8(q8, static_cast<const uint16_t*>(da_f16),
-                                              static_cast<const int16_t*>(ssum), m, k, ldx, workspace, true, stream));
+                                              static_cast<const int16_t*>(ssum), m, k, ldx, workspace, stream));
         }
         if (st != Q4K_OK) return st;
         return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream,

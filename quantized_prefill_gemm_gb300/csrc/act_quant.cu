@@ -165,26 +165,18 @@ __global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_kernel(const float* 
     ssum[t * kc + c] = static_cast<int16_t>(b.ssum);
 }
 
-// Two q8 codes as an exact 16-bit pair: fp16 (the Q4_K GEMM's operand) or
-// bf16 (the Q6_K GEMM's: its weight planes are bf16, and an MMA takes one type).
-template <bool kBf16>
+// Two q8 codes as an exact fp16 pair (the GEMM operand of both weight formats).
 __device__ __forceinline__ uint32_t code_pair(int q0, int q1) {
-    if constexpr (kBf16) {
-        const __nv_bfloat162 pr = __floats2bfloat162_rn(static_cast<float>(q0), static_cast<float>(q1));
-        return *reinterpret_cast<const uint32_t*>(&pr);
-    } else {
-        const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-        return *reinterpret_cast<const uint32_t*>(&pr);
-    }
+    const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+    return *reinterpret_cast<const uint32_t*>(&pr);
 }
 
-template <bool kBf16>
 __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64_t m, int64_t k, int64_t kc,
                                               const int (&q)[4], __half da, int ssum, uint16_t* __restrict__ xq,
                                               float* __restrict__ dat, __nv_bfloat16* __restrict__ e) {
     uint2 w;
-    w.x = code_pair<kBf16>(q[0], q[1]);
-    w.y = code_pair<kBf16>(q[2], q[3]);
+    w.x = code_pair(q[0], q[1]);
+    w.y = code_pair(q[2], q[3]);
     *reinterpret_cast<uint2*>(xq + t * k + c * 32 + 4 * j) = w;
     if (j == 0) {
         dat[((t >> 7) * kc + c) * 128 + (t & 127)] = __half2float(da);
@@ -195,15 +187,13 @@ __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64
     }
 }
 
-// GEMM operand form (see q4k_layout.h; codes as fp16, or bf16 with kBf16)
-// from fp32 activations.  A warp takes 8 consecutive 32-k blocks of one token
+// GEMM operand form (see q4k_layout.h; fp16 codes) from fp32 activations.  A warp takes 8 consecutive 32-k blocks of one token
 // (1 KB of fp32; k is a multiple of 256, so the blocks of a token come in
 // whole eights), and an 8-lane group one block per 16-B load: each load
 // instruction reads 512 contiguous bytes, each code store writes 256, and the
 // lane's two loads are in flight together.  The input is read once, so it is
 // loaded with the evict-first hint and leaves L2 to the operand the GEMM
 // reads next.
-template <bool kBf16>
 __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float* __restrict__ x, int64_t m,
                                                                      int64_t mp, int64_t k, int64_t ldx,
                                                                      uint16_t* __restrict__ xq,
@@ -228,12 +218,11 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float
     const float4 v0 = __ldcs(src + lane), v1 = __ldcs(src + 32 + lane);
     const LaneQ8 r0 = quantize_lane(v0);
     const LaneQ8 r1 = quantize_lane(v1);
-    write_operand<kBf16>(t, c0 + b, j, m, k, kc, r0.q, r0.da, r0.ssum, xq, dat, e);
-    write_operand<kBf16>(t, c0 + 4 + b, j, m, k, kc, r1.q, r1.da, r1.ssum, xq, dat, e);
+    write_operand(t, c0 + b, j, m, k, kc, r0.q, r0.da, r0.ssum, xq, dat, e);
+    write_operand(t, c0 + 4 + b, j, m, k, kc, r1.q, r1.da, r1.ssum, xq, dat, e);
 }
 
 // GEMM operand form from the public q8 SoA ([m][ldq] int8, da, ssum [m][kc]).
-template <bool kBf16>
 __global__ void __launch_bounds__(kThreadsPerBlock) act_from_q8_kernel(const int8_t* __restrict__ q8,
                                                                        const uint16_t* __restrict__ da,
                                                                        const int16_t* __restrict__ ssum, int64_t m,
@@ -258,7 +247,7 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_from_q8_kernel(const int
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = static_cast<int>(static_cast<int8_t>((w >> (8 * i)) & 0xFFu));
     const __half dh = __ushort_as_half(da[t * kc + c]);
-    write_operand<kBf16>(t, c, j, m, k, kc, q, dh, static_cast<int>(ssum[t * kc + c]), xq, dat, e);
+    write_operand(t, c, j, m, k, kc, q, dh, static_cast<int>(ssum[t * kc + c]), xq, dat, e);
 }
 
 inline unsigned grid_for(int64_t threads) {
@@ -280,8 +269,7 @@ cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_
                       ssum);
 }
 
-cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, bool bf16,
-                                cudaStream_t s) {
+cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s) {
     const ActLayout L(m, k);
     const int64_t mp = align_up(m, kTileM);
     const int64_t threads = mp * (k / 32) * 4;   // a warp per 8 blocks of a token
@@ -290,14 +278,12 @@ cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ld
     uint16_t* xq = reinterpret_cast<uint16_t*>(b + L.xq);
     float* dat = reinterpret_cast<float*>(b + L.da);
     __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(b + L.e);
-    return bf16 ? launch_pdl(act_quant_kernel<true>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp,
-                             k, ldx, xq, dat, e)
-                : launch_pdl(act_quant_kernel<false>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp,
-                             k, ldx, xq, dat, e);
+    return launch_pdl(act_quant_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, x, m, mp, k, ldx, xq,
+                      dat, e);
 }
 
 cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
-                               int64_t ldq, void* ws, bool bf16, cudaStream_t s) {
+                               int64_t ldq, void* ws, cudaStream_t s) {
     const ActLayout L(m, k);
     const int64_t mp = align_up(m, kTileM);
     const int64_t threads = mp * (k / 32) * 8;
@@ -306,10 +292,8 @@ cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16
     uint16_t* xq = reinterpret_cast<uint16_t*>(b + L.xq);
     float* dat = reinterpret_cast<float*>(b + L.da);
     __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(b + L.e);
-    return bf16 ? launch_pdl(act_from_q8_kernel<true>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da,
-                             ssum, m, mp, k, ldq, xq, dat, e)
-                : launch_pdl(act_from_q8_kernel<false>, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da,
-                             ssum, m, mp, k, ldq, xq, dat, e);
+    return launch_pdl(act_from_q8_kernel, dim3(grid_for(threads)), dim3(kThreadsPerBlock), 0, s, q8, da, ssum, m, mp,
+                      k, ldq, xq, dat, e);
 }
 
 }  // namespace q4k

@@ -54,8 +54,8 @@ constexpr int kThreads = 512;
 
 // Shared-memory carve-out per format.  Q4_K: three stages of 128 k (four
 // 32-k chunks) holding the fp16 A tile, the fp16 B tile (sc*q), the packed
-// quants, sc and d.  Q6_K: four stages of 64 k (the B tile has two bf16
-// planes, hi and lo) plus the high quant bits.  A and B tiles are made of
+// quants, sc and d.  Q6_K: four stages of 64 k (the B tile has two fp16
+// planes, the sh and the sl part of the scale) plus the high quant bits.  A and B tiles are made of
 // 16 KB boxes of 128 rows x 64 k (128-B rows, 128-B swizzle), one per two
 // chunks.  A min-term stage uses as many boxes of A and B, each 64 deep.
 template <bool kQ6>
@@ -65,7 +65,7 @@ struct Lay {
     static constexpr int kStages = kQ6 ? 4 : 3;
     static constexpr uint32_t kBox = 16384;                     // 128 rows x 64 fp16 / bf16
     static constexpr uint32_t kStageA = kBox * (kCh / 2);
-    static constexpr uint32_t kStageB = kQ6 ? 2 * kBox : kBox * (kCh / 2);   // Q6_K: hi plane, then lo plane
+    static constexpr uint32_t kStageB = kQ6 ? 2 * kBox : kBox * (kCh / 2);   // Q6_K: sh plane, then sl plane
     static constexpr uint32_t kStageNib = 2048 * kCh;           // chunks x 128 rows x 16 B
     static constexpr uint32_t kStageHi = kQ6 ? 1024 * kCh : 0;  // chunks x 128 rows x 8 B
     static constexpr uint32_t kStageSc = (kQ6 ? 256 : 128) * kCh;   // chunks x 128 rows x (2 or 1) B
@@ -299,12 +299,12 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t tj = tg + 128u * h;
-                        if constexpr (kQ6) {   // bf16: the hi plane, then the lo plane, into one accumulator
+                        if constexpr (kQ6) {   // fp16: the sh plane, then the sl plane, into one accumulator
                             const uint64_t bl = sw128_kmajor_desc(cx.b(s) + L::kStageB / 2);
-                            tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMin, 0u);
-                            tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMin, 1u);
-                            tc_mma_f16(tj, ad + 4u * h, bl + 4u * h, kIdescMin, 1u);
-                            tc_mma_f16(tj, ad + 4u * h + 2u, bl + 4u * h + 2u, kIdescMin, 1u);
+                            tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
+                            tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
+                            tc_mma_f16(tj, ad + 4u * h, bl + 4u * h, kIdescMain, 1u);
+                            tc_mma_f16(tj, ad + 4u * h + 2u, bl + 4u * h + 2u, kIdescMain, 1u);
                         } else {
                             tc_mma_f16(tj, ad + 4u * h, bd + 4u * h, kIdescMain, 0u);
                             tc_mma_f16(tj, ad + 4u * h + 2u, bd + 4u * h + 2u, kIdescMain, 1u);
@@ -331,53 +331,65 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
 }
 
 // ------------------------------------------------------------ converters --
-// Q6_K: row r of stage s.  Each weight's exact integer a = sc * (q - 32)
-// (|a| <= 4096, exact in fp32) becomes hi = bf16(a) and lo = a - hi (exact
-// in bf16); the two bf16 planes go to the two halves of the B tile, so that
-// two MMAs per 16 k add hi*qa + lo*qa = a*qa into the accumulator.  With
-// max |hi| + |lo| = 4096 over all (sc, q), every partial sum of a 32-k
-// chunk stays below 32 * 4096 * 127 < 2^24: the chunk integer is exact.
+// Q6_K: row r of stage s.  Each weight's exact integer a = sc * (q - 32) is
+// split by its scale: sc = sh + sl with sl = sc & 7 and sh = sc - sl, a
+// multiple of 8.  Both parts are exact fp16 integers: sh * (q - 32) is 8 times
+// a product of magnitude <= 16 * 32 = 512, and |sl * (q - 32)| <= 224.  The two
+// fp16 planes go to the two halves of the B tile, so that two MMAs per 16 k add
+// (sh + sl) * (q - 32) * qa = a * qa into the accumulator; with
+// |sh * v| + |sl * v| <= 4096 every partial sum of a 32-k chunk stays below
+// 32 * 4096 * 127 < 2^24: the chunk integer is exact.  A pair of weights is
+// built as fp16(64 + q), the bit pattern 0x5400 | q << 4, straight from the
+// packed words, and each plane is one fused multiply-add
+// (64 + q) * s - 96 * s = s * (q - 32): exact, since 96 * s and the result are
+// fp16 integers.
 template <bool kQ6>
 __device__ __forceinline__ void convert_q6(const Ctx<kQ6>& cx, int s, int r, uint32_t rx, uint32_t row_off) {
     using L = Lay<kQ6>;
     const uint8_t* lo = cx.sbase + L::kOffNib + L::kStageNib * s;
     const uint8_t* hi = cx.sbase + L::kOffHi + L::kStageHi * s;
     const uint8_t* scs = cx.sbase + L::kOffSc + L::kStageSc * s;
-    uint8_t* bhi = cx.sbase + L::kOffB + L::kStageB * s + row_off;
-    uint8_t* blo = bhi + L::kStageB / 2;
-    const __nv_bfloat162 m160 = __float2bfloat162_rn(-160.0f);
+    uint8_t* bh = cx.sbase + L::kOffB + L::kStageB * s + row_off;   // the sh plane
+    uint8_t* bl = bh + L::kStageB / 2;                                 // the sl plane
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const uint4 wl = *reinterpret_cast<const uint4*>(lo + (h * 128 + r) * 16);
         const uint2 wh = *reinterpret_cast<const uint2*>(hi + (h * 128 + r) * 8);
         const uint32_t scp = *reinterpret_cast<const uint16_t*>(scs + (h * 128 + r) * 2);
-        // the scales as bf16 pairs (exact: |sc| <= 128)
-        const __nv_bfloat162 sc0 = __float2bfloat162_rn(static_cast<float>(static_cast<int8_t>(scp & 0xFFu)));
-        const __nv_bfloat162 sc1 = __float2bfloat162_rn(static_cast<float>(static_cast<int8_t>(scp >> 8)));
+        __half2 sh2[2], sl2[2], ch2[2], cl2[2];   // per 16-weight sub-block: the two parts and -96 times them
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int sc = static_cast<int8_t>((scp >> (8 * b)) & 0xFFu);
+            const int sl = sc & 7, sh = sc - sl;
+            sh2[b] = __half2half2(__int2half_rn(sh));
+            sl2[b] = __half2half2(__int2half_rn(sl));
+            ch2[b] = __half2half2(__int2half_rn(-96 * sh));
+            cl2[b] = __half2half2(__int2half_rn(-96 * sl));
+        }
         const uint32_t lw[4] = {wl.x, wl.y, wl.z, wl.w};
         const uint32_t hw[4] = {wh.x, wh.x >> 2, wh.y, wh.y >> 2};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {   // 8-k group i of chunk h
-            const __nv_bfloat162 sc = i < 2 ? sc0 : sc1;
-            uint32_t ohi[4], olo[4];
+            const int b = i >> 1;
+            uint32_t oh[4], ol[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                // the pair k = 2jj, 2jj+1 straight from the packed words: the low
-                // nibbles sit at bits 4jj and 16+4jj, the 2-bit high fields at the
-                // same places of the shifted high-bit word.  bf16(128 + q) is the
-                // pattern 0x4300 | q; the stored field is u = q ^ 32, so bit 5 is
-                // flipped with the exponent bits in one step.  Minus 160: v = q - 32, exact.
-                const uint32_t hf = jj == 0 ? (hw[i] << 4) : (hw[i] >> (4 * jj - 4));
-                const uint32_t raw = ((lw[i] >> (4 * jj)) & 0x000F000Fu) | ((hf & 0x00300030u) ^ 0x43204320u);
-                const __nv_bfloat162 v = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&raw), m160);
-                const __nv_bfloat162 h2 = __hmul2(v, sc);                 // hi = RN_bf16(sc * v)
-                const __nv_bfloat162 l2 = __hfma2(v, sc, __hneg2(h2));    // lo = sc * v - hi, exact
-                ohi[jj] = *reinterpret_cast<const uint32_t*>(&h2);
-                olo[jj] = *reinterpret_cast<const uint32_t*>(&l2);
+                // the pair k = 2jj, 2jj+1: low nibbles at bits 4jj and 16+4jj of the
+                // quant word, 2-bit high fields at the same places of the shifted
+                // high-bit word; moved to mantissa bits 4-9.  The stored field is
+                // u = q ^ 32, so bit 9 is flipped with the exponent bits in one step.
+                const uint32_t lf = jj == 0 ? (lw[i] << 4) : (lw[i] >> (4 * jj - 4));
+                const uint32_t hf = jj < 2 ? (hw[i] << (8 - 4 * jj)) : (hw[i] >> (4 * jj - 8));
+                const uint32_t raw = (lf & 0x00F000F0u) | ((hf & 0x03000300u) ^ 0x56005600u);
+                const __half2 v = *reinterpret_cast<const __half2*>(&raw);   // 64 + q
+                const __half2 ph = __hfma2(v, sh2[b], ch2[b]);              // sh * (q - 32)
+                const __half2 pl = __hfma2(v, sl2[b], cl2[b]);              // sl * (q - 32)
+                oh[jj] = *reinterpret_cast<const uint32_t*>(&ph);
+                ol[jj] = *reinterpret_cast<const uint32_t*>(&pl);
             }
             const uint32_t g = static_cast<uint32_t>(4 * h + i);
-            *reinterpret_cast<uint4*>(bhi + ((g ^ rx) << 4)) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-            *reinterpret_cast<uint4*>(blo + ((g ^ rx) << 4)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+            *reinterpret_cast<uint4*>(bh + ((g ^ rx) << 4)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+            *reinterpret_cast<uint4*>(bl + ((g ^ rx) << 4)) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
         }
     }
 }
@@ -719,7 +731,7 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
 // kDump: also write every per-chunk accumulator to p.dbg (test hook build).
 // kSwiGLU: gate/up pair weights; the tile end writes the down projection's
 // q8 operand of SiLU(gate)*up instead of Y.
-// kQ6: Q6_K weights (Q6Layout) and a bf16 activation operand.
+// kQ6: Q6_K weights (Q6Layout), two fp16 weight planes per stage.
 template <bool kDump, bool kSwiGLU, bool kQ6>
 __global__ void __launch_bounds__(kThreads, 1)
     q4k_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_e,

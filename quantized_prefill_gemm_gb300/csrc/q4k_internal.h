@@ -89,11 +89,10 @@ struct GemvParams {
 
 cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8,
                                     uint16_t* da, int16_t* ssum, cudaStream_t s);
-// The GEMM operand form in ws (ActLayout); bf16 codes for the Q6_K GEMM, fp16 otherwise.
-cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, bool bf16,
-                                cudaStream_t s);
+// The GEMM operand form in ws (ActLayout): fp16 codes, d_a, and the bf16 hi/lo of d_a * ssum.
+cudaError_t launch_act_quantize(const float* x, int64_t m, int64_t k, int64_t ldx, void* ws, cudaStream_t s);
 cudaError_t launch_act_from_q8(const int8_t* q8, const uint16_t* da, const int16_t* ssum, int64_t m, int64_t k,
-                               int64_t ldq, void* ws, bool bf16, cudaStream_t s);
+                               int64_t ldq, void* ws, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);
 // Q6_K blocks [n][k/256] x 210 B -> Q6Layout (small-M path)
 cudaError_t launch_pack_q6k(const uint8_t* blocks, int64_t n, int64_t k, uint8_t* packed, cudaStream_t s);

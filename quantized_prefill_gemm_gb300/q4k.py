@@ -333,7 +333,7 @@ def q4k_gemm_debug_chunk_acc(packed, n, k, workspace, m, stream=None):
 
 
 def q6k_gemm_debug_chunk_acc(packed, n, k, workspace, m, stream=None):
-    """Test hook for Q6_K (workspace: the bf16 operand a q6k_gemm call with m > 16 left in it):
+    """Test hook for Q6_K (workspace: the operand form a q6k_gemm call with m > 16 left in it):
     (y fp32 [m][n], J fp32 [m][n][k/32]) with J the exact per-chunk integers."""
     y = torch.empty((m, n), dtype=torch.float32, device=packed.device)
     acc = torch.zeros((m, n, k // 32), dtype=torch.float32, device=packed.device)
