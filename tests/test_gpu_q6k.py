@@ -125,3 +125,36 @@ def test_small_m_too_large_for_shared_memory_takes_tensor_path(q4k):
     """16 tokens x 14336 do not fit the small-M kernel's shared memory: the
     call takes the tensor-core path instead and stays correct."""
     _check(q4k, 256, 14336, 16, 3, out="f32", act="f32")
+
+
+def test_prefill_extreme_scales_exact(q4k):
+    """The worst cases of the tensor-core path's exactness argument: rows with
+    sc = -128 and q = 0 (sc * (q - 32) = 4096), sc = 127 and q = 63, sc = -128
+    and q = 63, against tokens whose codes are all +127 or alternate +-127, so
+    that a chunk's partial sums reach 32 * 4096 * 127 = 16,646,144 < 2^24.
+    Every per-chunk integer equals the oracle's, every output is in bound."""
+    m, n, k = 64, 128, 256
+    q = np.zeros((n, k), dtype=np.uint8)
+    sc = np.zeros((n, k // 16), dtype=np.int8)
+    q[0:32], sc[0:32] = 0, -128
+    q[32:64], sc[32:64] = 63, 127
+    q[64:96], sc[64:96] = 63, -128
+    rng = np.random.default_rng(17)
+    q[96:] = rng.integers(0, 64, (32, k))
+    sc[96:] = rng.integers(-128, 128, (32, k // 16))
+    d_bits = np.full((n, k // 256), 0x1400, dtype=np.uint16)   # f16 2^-10
+    blocks = oq6.encode(q, sc, d_bits)
+    x = np.ones((m, k), dtype=np.float32)
+    x[32:] *= np.where(np.arange(k) % 2 == 0, 1.0, -1.0).astype(np.float32)   # codes +127 / alternating
+    packed = q4k.q6k_pack_weights(to_dev(blocks), n, k)
+    ws = torch.empty(q4k.q4k_act_workspace_bytes(m, k), dtype=torch.uint8, device=DEV)
+    y = q4k.q6k_gemm(packed, n, k, to_dev(x), out_dtype="f32", workspace=ws)
+    _, acc = q4k.q6k_gemm_debug_chunk_acc(packed, n, k, ws, m)
+    torch.cuda.synchronize()
+    f = oq6.decode(blocks)
+    qa, _, _ = oq8.quantize_rows(x)
+    ints = oq6.chunk_ints(f, qa)
+    assert ints[0, 0, 0] == 32 * 4096 * 127
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ints)
+    want, scale = _oracle(blocks, x)
+    assert_close(y.float().cpu().double().numpy(), want, scale, "f32", "q6k extreme scales")
