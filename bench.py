@@ -292,7 +292,7 @@ def main():
 
     def step(events=None):
         for i, (n, k) in enumerate(mats):
-            if q6:   # q6k_gemm quantizes into ws (bf16 operand) and runs the GEMM: the events take both
+            if q6:   # q6k_gemm quantizes into ws (fp16 operand) and runs the GEMM: the events take both
                 if events is not None:
                     events[i][0].record(stream)
                 q4k.q6k_gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws, stream=stream)
@@ -339,7 +339,7 @@ def main():
                 "traffic": traffic, "traffic_unit": "bytes per launch",
                 "kernel": "q4k_gemm_kernel" + ("<Q6_K>" if q6 else ""),
                 "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step); the GEMM issues "
-                               + ("bf16" if q6 else "f16") + " tcgen05 MMAs, same rate class",
+                               "f16 tcgen05 MMAs, same rate class",
                 "per_launch": "2*M*N*K algorithmic flops / CUDA-event duration of each GEMM launch"}
 
     e2e = None
@@ -350,7 +350,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("bf16 x bf16 -> f32 tensor-core MMA on exact q6/q8 integers (hi/lo weight planes)" if q6
+            "dtype": ("f16 x f16 -> f32 tensor-core MMA on exact q6/q8 integers (two weight planes split by the scale)" if q6
                       else "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers"),
             "data": "synthetic (seeded random {} weights and activations)".format("Q6_K" if q6 else "Q4_K"),
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),

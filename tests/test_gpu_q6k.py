@@ -81,21 +81,21 @@ def test_in_kernel_quantization_bits(q4k, m):
 @pytest.mark.parametrize("m,n,k,out,act", [(17, 128, 256, "f32", "f32"), (64, 256, 512, "f32", "q8"),
                                             (200, 384, 768, "bf16", "f32"), (300, 256, 2816, "f32", "q8")])
 def test_prefill_sizes_tensor_core_path(q4k, m, n, k, out, act):
-    """m > 16: the tcgen05 GEMM with bf16 hi/lo weight planes (every output,
+    """m > 16: the tcgen05 GEMM with two fp16 weight planes (every output,
     ragged token tiles, the k-split of the last wave)."""
     _check(q4k, n, k, m, 90 + m, out=out, act=act, kind="outlier")
 
 
 def test_prefill_chunk_integers_exact(q4k):
     """Every per-chunk accumulator of the tensor-core path equals the oracle's
-    exact integer sum_s sc_s * sum (q - 32) * qa: the hi/lo split and the fp32
-    accumulator lose nothing."""
+    exact integer sum_s sc_s * sum (q - 32) * qa: the split of sc into its high
+    and low bits and the fp32 accumulator lose nothing."""
     m, n, k = 64, 256, 512
     blocks = inputs.q6k_blocks(n, k, 5)
     x = inputs.activations(m, k, 5, "outlier")
     packed = q4k.q6k_pack_weights(to_dev(blocks), n, k)
     ws = torch.empty(q4k.q4k_act_workspace_bytes(m, k), dtype=torch.uint8, device=DEV)
-    y = q4k.q6k_gemm(packed, n, k, to_dev(x), workspace=ws)   # leaves the bf16 operand in ws
+    y = q4k.q6k_gemm(packed, n, k, to_dev(x), workspace=ws)   # leaves the fp16 operand in ws
     y2, acc = q4k.q6k_gemm_debug_chunk_acc(packed, n, k, ws, m)
     torch.cuda.synchronize()
     f = oq6.decode(blocks)
