@@ -28,7 +28,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // 32-k chunks per main stage of the tensor-core GEMM: 4 (128 k) for Q4_K,
-// 2 (64 k) for Q6_K, whose stages carry two bf16 weight planes.
+// 2 (64 k) for Q6_K, whose stages carry two fp16 weight planes.
 __host__ __device__ constexpr int gemm_chunks_per_stage(bool q6) { return q6 ? 2 : 4; }
 
 struct GemmParams {
@@ -59,7 +59,7 @@ struct GemmParams {
     __nv_bfloat16* he;      // [2][m][kd/32] d_a*ssum hi / lo
     int hkc;                // kd / 32
     // Q6_K weights (Q6Layout: nib = low nibbles, sc = i8 scale pairs,
-    // dsb = d) with a bf16 activation operand; no min term
+    // dsb = d) with the fp16 activation operand; no min term
     const uint8_t* q6hi;    // the high quant bits [nt][kc][128][8 B]
     int q6;
 };

@@ -183,6 +183,26 @@ def test_k_split_tail_and_workspace_reuse(q4k):
     assert_close(ys[0].cpu().double().numpy(), want, scale, "f32", "k-split tail")
 
 
+def test_k_split_four_parts_ragged_token_tile(q4k):
+    """200 tokens x 11520 outputs: 2 x 90 = 180 tiles, a whole wave of 152 and
+    28 tail tiles, each split along k into 4 parts of 4 super-blocks (only
+    the first with the min term); the second token tile is ragged, so the
+    fixup meets padding rows.  Sampled token rows of both tiles against the
+    oracle, in both output types, and the bits repeat."""
+    m, n, k = 200, 11520, 4096
+    blocks, x = make_case(n, k, m, "outlier", seed=77)
+    packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+    ws = q4k.q4k_act_quantize(to_dev(x))
+    y32 = [q4k.q4k_gemm_quantized(packed, n, k, ws, m, "f32") for _ in range(2)]
+    y16 = q4k.q4k_gemm_quantized(packed, n, k, ws, m, "bf16")
+    torch.cuda.synchronize()
+    assert torch.equal(y32[0], y32[1])
+    rows = np.array([0, 77, 127, 128, 163, 199])
+    want, scale = oracle_rows(blocks, x, rows)
+    assert_close(y32[0].cpu().double().numpy()[rows], want, scale, "f32", "4-way split f32")
+    assert_close(y16.float().cpu().double().numpy()[rows], want, scale, "bf16", "4-way split bf16")
+
+
 def test_long_k_min_term_boxes_and_exact_chunks(q4k):
     """K = 14336 (448 chunks): 112 main stages of 128 k and 12 min-term stages,
     whose last depth block holds one box partly and one wholly past kc (read as
