@@ -538,48 +538,73 @@ def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, s
             "overlap": "one input copy, the products, one output copy per step, replayed from a CUDA graph"}
 
 
-def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2, gemm=None):
+def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=3, gemm=None, group=7):
     """Same metric through the public fused call q4k_gemm, with every
     projection's activations copied from pinned host memory and its result
-    copied back inside the timed region.  As a serving loop would, the copies
-    run on their own streams (host->device, device->host) with two device
-    buffers per shape, so that projection i+1's input and projection i-1's
-    output move while projection i computes; events order every buffer reuse."""
-    host_x = []
-    for x in xs:
-        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-        hx.copy_(x)
-        host_x.append(hx)
+    copied back inside the timed region.  The copies are batched per group of
+    `group` consecutive projections (one layer of the 7B stack) when a step
+    holds at least four such groups: one host->device copy brings a group's
+    inputs, one device->host copy takes its outputs back.  They run on their
+    own streams with two device buffer sets, so that group j+1's inputs and
+    group j-1's outputs move while group j computes; events order every
+    buffer reuse.  The compute stream meets those events only between groups:
+    an event between two kernels ends their programmatic-dependent-launch
+    overlap, which per-projection copies would cost the stack about a
+    millisecond per step.  A shorter step copies per projection, since the
+    first group's inputs and the last group's outputs cannot overlap any
+    compute of the step."""
+    if len(mats) < 4 * group:
+        group = 1
     ydt = torch.bfloat16 if out == "bf16" else torch.float32
-    host_y = [torch.empty((tokens, n), dtype=ydt, pin_memory=True) for n, _ in mats]
+    groups = [list(range(i, min(i + group, len(mats)))) for i in range(0, len(mats), group)]
+    host_x, host_y, xoffs, yoffs, sigs = [], [], [], [], []
+    for gi in groups:
+        xo, yo = [0], [0]
+        for i in gi:
+            n, k = mats[i]
+            xo.append(xo[-1] + tokens * k)
+            yo.append(yo[-1] + tokens * n)
+        hx = torch.empty(xo[-1], dtype=torch.float32, pin_memory=True)
+        for j, i in enumerate(gi):
+            hx[xo[j]:xo[j + 1]].copy_(xs[i].reshape(-1))
+        host_x.append(hx)
+        host_y.append(torch.empty(yo[-1], dtype=ydt, pin_memory=True))
+        xoffs.append(xo)
+        yoffs.append(yo)
+        sigs.append(tuple(mats[i] for i in gi))
     nbuf = 2
-    dx = {k: [torch.empty((tokens, k), dtype=torch.float32, device=dev) for _ in range(nbuf)] for _, k in mats}
-    dy = {n: [torch.empty((tokens, n), dtype=ydt, device=dev) for _ in range(nbuf)] for n, _ in mats}
-    x_free = {k: [torch.cuda.Event() for _ in range(nbuf)] for k in dx}   # the GEMM that read it is done
-    y_free = {n: [torch.cuda.Event() for _ in range(nbuf)] for n in dy}   # its copy to the host is done
+    dx = {sg: [torch.empty(xoffs[j][-1], dtype=torch.float32, device=dev) for _ in range(nbuf)]
+          for j, sg in enumerate(sigs)}
+    dy = {sg: [torch.empty(yoffs[j][-1], dtype=ydt, device=dev) for _ in range(nbuf)] for j, sg in enumerate(sigs)}
+    x_free = {sg: [torch.cuda.Event() for _ in range(nbuf)] for sg in dx}   # the GEMMs that read it are done
+    y_free = {sg: [torch.cuda.Event() for _ in range(nbuf)] for sg in dy}   # its copy to the host is done
     h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     uses = {}
 
     def step():
-        for i, (n, k) in enumerate(mats):
-            bx = uses[("x", k)] = (uses.get(("x", k), -1) + 1) % nbuf
-            by = uses[("y", n)] = (uses.get(("y", n), -1) + 1) % nbuf
-            xb, yb = dx[k][bx], dy[n][by]
-            h2d.wait_event(x_free[k][bx])
+        for j, gi in enumerate(groups):
+            sg = sigs[j]
+            b = uses[sg] = (uses.get(sg, -1) + 1) % nbuf
+            xb, yb = dx[sg][b], dy[sg][b]
+            h2d.wait_event(x_free[sg][b])
             with torch.cuda.stream(h2d):
-                xb.copy_(host_x[i], non_blocking=True)
+                xb.copy_(host_x[j], non_blocking=True)
             arrived = torch.cuda.Event()
             arrived.record(h2d)
             stream.wait_event(arrived)
-            stream.wait_event(y_free[n][by])
-            (gemm or q4k.q4k_gemm)(packed[i], n, k, xb, out_dtype=out, y=yb, workspace=ws, stream=stream)
-            x_free[k][bx].record(stream)
+            stream.wait_event(y_free[sg][b])
+            xo, yo = xoffs[j], yoffs[j]
+            for q, i in enumerate(gi):
+                n, k = mats[i]
+                (gemm or q4k.q4k_gemm)(packed[i], n, k, xb[xo[q]:xo[q + 1]].view(tokens, k), out_dtype=out,
+                                       y=yb[yo[q]:yo[q + 1]].view(tokens, n), workspace=ws, stream=stream)
+            x_free[sg][b].record(stream)
             done = torch.cuda.Event()
             done.record(stream)
             d2h.wait_event(done)
             with torch.cuda.stream(d2h):
-                host_y[i].copy_(yb, non_blocking=True)
-            y_free[n][by].record(d2h)
+                host_y[j].copy_(yb, non_blocking=True)
+            y_free[sg][b].record(d2h)
 
     step()
     torch.cuda.synchronize()
@@ -598,7 +623,8 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=2,
     d2h_bytes = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
     return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d_bytes,
             "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ms, "steps": steps,
-            "overlap": "copies on their own streams, two device buffers per shape"}
+            "overlap": (f"copies batched per {group} projections" if group > 1 else "copies per projection")
+                       + " on their own streams, two device buffer sets"}
 
 
 def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream):
