@@ -23,8 +23,8 @@
 // output tile at a time, k in stages of 128 for Q4_K and 64 for Q6_K (four or
 // two chunks of 32):
 //   warp 0        TMA producer: activation tile (fp16, 128-B swizzle), packed
-//                 quants, sc, and d at super-block ends; for the min-term
-//                 stages the bf16 E and -(dmin*m) tiles
+//                 quants and sc; d at super-block ends, into a ring of its
+//                 own; for the min-term stages the bf16 E and -(dmin*m) tiles
 //   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk, two chunks into
 //                 the two accumulators of one TMEM group, one commit for both;
 //                 4 bf16 MMAs per 64 of min-term depth into a group's first one
@@ -54,10 +54,13 @@ constexpr int kThreads = 512;
 
 // Shared-memory carve-out per format.  Q4_K: three stages of 128 k (four
 // 32-k chunks) holding the fp16 A tile, the fp16 B tile (sc*q), the packed
-// quants, sc and d.  Q6_K: four stages of 64 k (the B tile has two fp16
+// quants and sc.  Q6_K: four stages of 64 k (the B tile has two fp16
 // planes, the sh and the sl part of the scale) plus the high quant bits.  A and B tiles are made of
 // 16 KB boxes of 128 rows x 64 k (128-B rows, 128-B swizzle), one per two
 // chunks.  A min-term stage uses as many boxes of A and B, each 64 deep.
+// The super-block scales d have a ring of their own, shared by the producer
+// and the drain only, so that the drain (the slowest role) never holds a
+// stage of the main ring.
 template <bool kQ6>
 struct Lay {
     static constexpr int kCh = gemm_chunks_per_stage(kQ6);     // 32-k chunks per main stage
@@ -69,22 +72,25 @@ struct Lay {
     static constexpr uint32_t kStageNib = 2048 * kCh;           // chunks x 128 rows x 16 B
     static constexpr uint32_t kStageHi = kQ6 ? 1024 * kCh : 0;  // chunks x 128 rows x 8 B
     static constexpr uint32_t kStageSc = (kQ6 ? 256 : 128) * kCh;   // chunks x 128 rows x (2 or 1) B
-    static constexpr uint32_t kStageD = 512;                    // 128 rows x fp32 (last stage of a super-block)
+    static constexpr uint32_t kSlotD = 512;                     // 128 rows x fp32, one super-block
+    static constexpr int kDRing = 4;                            // d slots (super-blocks in flight)
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + kStages * kStageA;
     static constexpr uint32_t kOffNib = kOffB + kStages * kStageB;
     static constexpr uint32_t kOffHi = kOffNib + kStages * kStageNib;
     static constexpr uint32_t kOffSc = kOffHi + kStages * kStageHi;
     static constexpr uint32_t kOffD = kOffSc + kStages * kStageSc;
-    static constexpr uint32_t kOffBar = kOffD + kStages * kStageD;
+    static constexpr uint32_t kOffBar = kOffD + kDRing * kSlotD;
     // barrier indices
     static constexpr int kBarFull = 0;                       // [kStages] producer -> all (tx bytes)
     static constexpr int kBarConv = kStages;                 // [kStages] converters -> MMA (4 arrivals)
-    static constexpr int kBarEmpty = 2 * kStages;            // [kStages] MMA commit + 8 drain arrivals -> producer
+    static constexpr int kBarEmpty = 2 * kStages;            // [kStages] MMA commit -> producer
     static constexpr int kBarAccFull = 3 * kStages;          // [2] MMA commit -> drain (one accumulator group)
     static constexpr int kBarAccEmpty = kBarAccFull + 2;     // [2] 8 drain warps -> MMA
     static constexpr int kBarDrain = kBarAccEmpty + 2;       // MMA's final commit
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarDFull = kBarDrain + 1;          // [kDRing] producer -> drain (tx bytes)
+    static constexpr int kBarDEmpty = kBarDFull + kDRing;    // [kDRing] 8 drain warps -> producer
+    static constexpr int kNumBars = kBarDEmpty + kDRing;
     static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
     static constexpr size_t kSmemBytes = kSmemUsed + 1024;          // + alignment slack
@@ -104,7 +110,7 @@ constexpr uint32_t kIdescMin = idesc_kind_f16(128, 128, true);     // bf16 x bf1
 // used: the running Y left TMEM, and with it the MMA's wait for a free Y)
 enum : unsigned {
     kSiteProdEmpty = 1, kSiteUnused2, kSiteMmaFull, kSiteMmaConv, kSiteMmaAccEmpty,
-    kSiteConvFull, kSiteEpiFull, kSiteEpiAccFull, kSiteEpiZ
+    kSiteConvFull, kSiteEpiD, kSiteEpiAccFull, kSiteEpiZ, kSiteProdD
 };
 
 template <bool kQ6>
@@ -132,6 +138,14 @@ __device__ __forceinline__ void advance(int& s, uint32_t& ph) {
     if (++s == Lay<kQ6>::kStages) {
         s = 0;
         ph ^= 1u;
+    }
+}
+
+template <bool kQ6>
+__device__ __forceinline__ void advance_d(int& ds, uint32_t& dph) {
+    if (++ds == Lay<kQ6>::kDRing) {
+        ds = 0;
+        dph ^= 1u;
     }
 }
 
@@ -177,14 +191,23 @@ template <bool kQ6>
 __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParams& p, const CUtensorMap* tm_x,
                                              const CUtensorMap* tm_e, const CUtensorMap* tm_d) {
     using L = Lay<kQ6>;
-    int s = 0;
+    int s = 0, ds = 0;
     uint32_t ph = 0, issued = 0, parity_bits = 0;
+    uint32_t dph = 0, d_issued = 0, d_parity_bits = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = unit_of<kQ6>(p, u);
         const int mt = w.mt, nt = w.nt;
         for (int st = 0; st < w.n_st; ++st) {
             if (!cx.wait(p, L::kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
+                ok = false;
+                break;
+            }
+            const int kb_ = st + w.kbase;
+            const bool sb_end = kb_ >= 0 && (kb_ + 1) % L::kStPerSb == 0;
+            // the last stage of a super-block also brings its d, into the d
+            // ring: its slot is taken before any copy of this stage is issued
+            if (sb_end && !cx.wait(p, L::kBarDEmpty + ds, dph ^ 1u, kSiteProdD)) {
                 ok = false;
                 break;
             }
@@ -201,10 +224,8 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
                     tma_load_3d(cx.b(s) + L::kBox * i, tm_d, fb, x, 128 * nt, part == 1 ? 1 : 0);
                 }
             } else {
-                const int kb = st + w.kbase;
-                const bool sb_last = (kb + 1) % L::kStPerSb == 0;
-                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageNib + L::kStageHi + L::kStageSc +
-                                              (sb_last ? L::kStageD : 0u));
+                const int kb = kb_;
+                mbar_arrive_expect_tx(fb, L::kStageA + L::kStageNib + L::kStageHi + L::kStageSc);
 #pragma unroll
                 for (int i = 0; i < L::kCh / 2; ++i)
                     tma_load_2d(cx.a(s) + L::kBox * i, tm_x, fb, 64 * (kb * (L::kCh / 2) + i), 128 * mt);
@@ -216,9 +237,15 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
                 } else {
                     bulk_load(cx.base + L::kOffSc + L::kStageSc * s, p.sc + rec * 128, L::kStageSc, fb);
                 }
-                if (sb_last)
-                    bulk_load(cx.base + L::kOffD + L::kStageD * s,
-                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + kb / L::kStPerSb) * 128, L::kStageD, fb);
+                if (sb_end) {
+                    const uint32_t dfb = cx.bar(L::kBarDFull + ds);
+                    mbar_arrive_expect_tx(dfb, L::kSlotD);
+                    bulk_load(cx.base + L::kOffD + L::kSlotD * ds,
+                              p.dsb + (static_cast<int64_t>(nt) * p.ksb + kb / L::kStPerSb) * 128, L::kSlotD, dfb);
+                    d_issued |= 1u << ds;
+                    d_parity_bits = (d_parity_bits & ~(1u << ds)) | (dph << ds);
+                    advance_d<kQ6>(ds, dph);
+                }
             }
             issued |= 1u << s;
             parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
@@ -228,6 +255,9 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
     if (!ok) {   // let every copy this thread started land before the CTA exits
         for (int i = 0; i < L::kStages; ++i)
             if ((issued >> i) & 1u) mbar_wait_quiet(cx.bar(L::kBarFull + i), (parity_bits >> i) & 1u, p.timeout_cycles);
+        for (int i = 0; i < L::kDRing; ++i)
+            if ((d_issued >> i) & 1u)
+                mbar_wait_quiet(cx.bar(L::kBarDFull + i), (d_parity_bits >> i) & 1u, p.timeout_cycles);
     }
 }
 
@@ -277,7 +307,6 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                         tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | i | kk) != 0 ? 1u : 0u);
                 }
                 tc_commit(cx.bar(L::kBarEmpty + s));
-                mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);   // the drain reads nothing of this stage
                 if (kb == -1) {   // Z complete: the group goes to the drain
                     tc_commit(cx.bar(L::kBarAccFull + g));
                     if (++g == 2) {
@@ -317,10 +346,7 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
                     }
                 }
                 if (!ok) break;
-                tc_commit(cx.bar(L::kBarEmpty + s));
-                // the drain reads a stage (its d) only at the end of a super-block;
-                // for every other stage this thread arrives in its place
-                if ((kb + 1) % L::kStPerSb != 0) mbar_arrive_cnt(cx.bar(L::kBarEmpty + s), 8);
+                tc_commit(cx.bar(L::kBarEmpty + s));   // the drain reads nothing of the main ring
             }
             advance<kQ6>(s, ph);
         }
@@ -582,17 +608,16 @@ __device__ __forceinline__ void store_partial(const GemmParams& p, const float* 
 // its warp index allows) and columns 64*(e/4)..+63 of each accumulator: each
 // thread owns one token row and 64 output columns.  Per main stage it folds
 // both chunks, P += d_a * J (packed fp32 FMA), and hands the group back after
-// its last TMEM load; per super-block Y += d * P; per unit Y -> HBM.  Of the
-// stage ring it joins only the super-block ends (to read d): the MMA thread
-// arrives in its place on every other stage.
+// its last TMEM load; per super-block Y += d * P, with d from the d ring
+// (it never waits on or releases a stage of the main ring); per unit Y -> HBM.
 template <bool kDump, bool kSwiGLU, bool kQ6>
 __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParams& p, int warp, int e, int lane) {
     using L = Lay<kQ6>;
     const int qd = warp & 3, ch = e >> 2;
     const int row = qd * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    int s = 0, g = 0;
-    uint32_t ph = 0, gph = 0;
+    int ds = 0, g = 0;
+    uint32_t dph = 0, gph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = unit_of<kQ6>(p, u);
@@ -688,12 +713,12 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
                     }
                 }
                 if (!ok) break;
-                if ((kb + 1) % L::kStPerSb == 0) {   // super-block done: Y += d * P, d from this stage
-                    if (!cx.warp_wait(p, L::kBarFull + s, ph, kSiteEpiFull)) {
+                if ((kb + 1) % L::kStPerSb == 0) {   // super-block done: Y += d * P, d from the d ring
+                    if (!cx.warp_wait(p, L::kBarDFull + ds, dph, kSiteEpiD)) {
                         ok = false;
                         break;
                     }
-                    const float* dv = reinterpret_cast<const float*>(cx.sbase + L::kOffD + L::kStageD * s) + 64 * ch;
+                    const float* dv = reinterpret_cast<const float*>(cx.sbase + L::kOffD + L::kSlotD * ds) + 64 * ch;
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
                         const float4 d4 = *reinterpret_cast<const float4*>(dv + j);
@@ -705,10 +730,10 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
 #pragma unroll
                     for (int j = 0; j < 64; ++j) P[j] = 0.0f;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(cx.bar(L::kBarEmpty + s));
+                    if (lane == 0) mbar_arrive(cx.bar(L::kBarDEmpty + ds));
+                    advance_d<kQ6>(ds, dph);
                 }
             }
-            advance<kQ6>(s, ph);
         }
         if (!ok) break;
         if (w.slot >= 0) {   // a k-part of a split tile: its partial Y, finished by the fixup kernel
@@ -751,7 +776,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(cx.bar(L::kBarFull + s), 1);
             mbar_init(cx.bar(L::kBarConv + s), 4);
-            mbar_init(cx.bar(L::kBarEmpty + s), 9);
+            mbar_init(cx.bar(L::kBarEmpty + s), 1);
+        }
+        for (int i = 0; i < L::kDRing; ++i) {
+            mbar_init(cx.bar(L::kBarDFull + i), 1);
+            mbar_init(cx.bar(L::kBarDEmpty + i), 8);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(cx.bar(L::kBarAccFull + b), 1);
