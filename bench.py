@@ -338,7 +338,7 @@ def main():
     achieved = flops_step / (gemm_ms * 1e-3) / 1e12
     # dram__bytes_read.sum + dram__bytes_write.sum of q4k_gemm_kernel per launch, averaged over the 224
     # launches of one stack step (ncu capture of this kernel version, summarized under profiles/)
-    traffic = 48.80e6 if args.workload == "stack" else None
+    traffic = 48.77e6 if args.workload == "stack" else None
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "traffic_unit": "bytes per launch",
                 "kernel": "q4k_gemm_kernel" + ("<Q6_K>" if q6 else ""),
