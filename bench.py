@@ -167,6 +167,13 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
+        return self.parse(out)
+
+    @staticmethod
+    def parse(out):
+        """The clock record from nvidia-smi's CSV lines (FIELDS, no header,
+        no units): median SM clock, the largest max clock, the throttle
+        reasons seen active in any sample, the sample count, peak power."""
         rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
         mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -540,6 +547,14 @@ def run_e2e_serial(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, s
             "overlap": "one input copy, the products, one output copy per step, replayed from a CUDA graph"}
 
 
+def copy_groups(n, group):
+    """The e2e copy batches: consecutive projection indices in groups of
+    `group` when there are at least four such groups, else one per group."""
+    if n < 4 * group:
+        group = 1
+    return [list(range(i, min(i + group, n))) for i in range(0, n, group)]
+
+
 def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=3, gemm=None, group=7):
     """Same metric through the public fused call q4k_gemm, with every
     projection's activations copied from pinned host memory and its result
@@ -555,10 +570,9 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=3,
     millisecond per step.  A shorter step copies per projection, since the
     first group's inputs and the last group's outputs cannot overlap any
     compute of the step."""
-    if len(mats) < 4 * group:
-        group = 1
+    groups = copy_groups(len(mats), group)
+    group = len(groups[0])
     ydt = torch.bfloat16 if out == "bf16" else torch.float32
-    groups = [list(range(i, min(i + group, len(mats)))) for i in range(0, len(mats), group)]
     host_x, host_y, xoffs, yoffs, sigs = [], [], [], [], []
     for gi in groups:
         xo, yo = [0], [0]

@@ -53,3 +53,27 @@ def test_hbm_view_fraction():
     v = bench.hbm_view({"hbm_gbs": 6669.5}, "measured", 26.2e6, 0.0608, "x")
     assert v["achieved"] == pytest.approx(26.2e6 / 60.8e-6 / 1e9)
     assert v["frac"] == pytest.approx(v["achieved"] / 6669.5)
+
+
+def test_copy_groups():
+    g = bench.copy_groups(224, 7)            # the 7B stack: one layer per copy
+    assert len(g) == 32 and all(len(x) == 7 for x in g)
+    assert [i for x in g for i in x] == list(range(224))
+    assert bench.copy_groups(8, 7) == [[i] for i in range(8)]       # too few layers: per projection
+    assert bench.copy_groups(3, 7) == [[0], [1], [2]]
+    g = bench.copy_groups(30, 7)             # a partial last group keeps every index once, in order
+    assert [len(x) for x in g] == [7, 7, 7, 7, 2] and [i for x in g for i in x] == list(range(30))
+
+
+def test_clock_record_parsing():
+    fields = bench.ClockSampler.FIELDS.split(",")
+    assert len(fields) == 8
+    line = "{}, 2070, {}, 0x0000000000000000, Not Active, Not Active, Not Active, {}"
+    out = "\n".join([line.format(2070, "350.10", "Not Active"), line.format(1980, "1390.00", "Active"),
+                     line.format(2070, "371.2", "Not Active"), "[N/A], [N/A]"])
+    rec = bench.ClockSampler.parse(out)
+    assert rec["sm_mhz"] == 2070 and rec["sm_max_mhz"] == 2070 and rec["samples"] == 3
+    assert rec["reasons"] == ["sw_power_cap"] and rec["power_w_max"] == 1390.0
+    hot = "1500, 2070, 300.0, 0x8, Not Active, Active, Not Active, Not Active"
+    assert bench.ClockSampler.parse(hot)["reasons"] == ["hw_thermal_slowdown"]
+    assert bench.ClockSampler.parse("")["sm_mhz"] is None
