@@ -24,11 +24,18 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
+BF16_U = 2.0 ** -8   # unit roundoff of bf16 (8 significant bits): |RN(v) - v| <= 2^-8 |v|
+
+
 def tolerance(y_or, scale, out):
-    """Acceptance bound per element: 1e-4 * sum|w*a| (+ one bf16 rounding for bf16 output)."""
+    """Acceptance bound per element: 1e-4 * sum|w*a| for fp32 output.
+
+    bf16 output is RN(y32) of an fp32 value y32 within 1e-4*S of the oracle,
+    so it adds one bf16 rounding of y32: |RN(y32) - y32| <= 2^-8 |y32| <=
+    2^-8 (|y_or| + 1e-4*S)."""
     tol = 1e-4 * scale
     if out == "bf16":
-        tol = tol + 2.0 ** -8 * np.abs(y_or)
+        tol = tol * (1.0 + BF16_U) + BF16_U * np.abs(y_or)
     return tol
 
 

@@ -1,13 +1,22 @@
 """Gate/up pair GEMM with the SiLU(gate)*up epilogue (q4k_gemm_swiglu),
 compared with the oracle.
 
-The q8 codes of h decide the down projection's input, so they are checked bit
-for bit: the oracle forms h from the same fp32 g and u the GPU product writes
-(the pair GEMM with f32 output; the epilogue reads the same accumulators), with
-its own fp32 SiLU in the fixed operation order, and quantizes it with its own
-q8 rule.  g and u themselves are checked against the oracle's exact GEMM with
-the usual bound, and the down projection fed from the epilogue's operand is
-checked end to end.
+Two checks, one per reading of what must match:
+
+* kernel specification: the q8 codes of h decide the down projection's input,
+  so they are checked bit for bit.  Here the oracle forms h from the same fp32
+  g and u the GPU product writes (the pair GEMM with f32 output; the epilogue
+  reads the same accumulators), with its own fp32 SiLU in the fixed operation
+  order, and quantizes it with its own q8 rule.  g and u themselves are checked
+  against the oracle's exact GEMM with the usual bound.
+* the FFN block from x alone (test_swiglu_chain_from_x_alone and the
+  full-size test): the oracle computes g and u blockwise from x, h with the
+  plain definition SiLU(g)*u = g/(1 + e^-g)*u in fp64, its q8 quantization and
+  the down product; nothing of it comes from the GPU.  The GPU's operand may
+  differ from the oracle's only where the error the GEMM bound allows in g and
+  u can move h across a q8 rounding boundary (chain_accept below), and the
+  down output must agree within the GEMM bound plus the exact effect of those
+  code steps.
 """
 import numpy as np
 import pytest
@@ -16,7 +25,7 @@ import torch
 from oracle import gemm as ogemm
 from oracle import q4k_blocks, q8 as oq8, swiglu as osw
 from quantized_prefill_gemm_gb300 import inputs
-from tests.gpu_common import DEV, assert_close, oracle_rows, sample_rows, to_dev
+from tests.gpu_common import BF16_U, DEV, assert_close, oracle_rows, sample_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +84,96 @@ def _check_operand(ws, h, rows, m):
     return qa, da_bits, ssum
 
 
+SILU_LIP = 1.0999   # max |d SiLU(g)/dg| over all g (1.0998 at g = 2.3994)
+EVAL_REL = 1e-6     # GPU fp32 SiLU*u vs the fp64 definition (test_oracle_swiglu pins 5e-7)
+U32 = 2.0 ** -24
+
+
+def gemm_error_bound(fields, qa, da_bits, ssum):
+    """Bound on |g_gpu - g| of the GPU product, from its arithmetic: the chunk
+    integers are exact; the fold, the super-block sum and the k-split sum are
+    at most 128 fp32 roundings, each within 2^-24 of S = sum|w*a|; the min term
+    Z = sum_c (d_a*ssum)(dmin*m) runs on bf16 hi/lo splits (each factor within
+    2^-16, so 3*2^-16 per product) accumulated in fp32 over 3*kc products
+    (2^-23 each, truncation allowed), relative to S_min = sum_c |d_a*ssum*dmin*m|."""
+    kc = qa.shape[1] // 32
+    s = ogemm.abs_scale(fields, qa, da_bits)
+    e = np.abs(oq8.f16_bits_to_f64(da_bits) * ssum.astype(np.float64))                 # [M][kc]
+    dmin = np.repeat(q4k_blocks.f16_bits_to_f64(fields["dmin_bits"]), 8, axis=1)        # [N][kc]
+    s_min = e @ (dmin * fields["m"].astype(np.float64)).T
+    return 128 * U32 * s + (3 * 2.0 ** -16 + 3 * kc * 2.0 ** -23) * s_min
+
+
+def chain_oracle(gate, up, down, x):
+    """The FFN block from x alone (fp64 wherever the pages fix no precision).
+
+    Returns (h, q8 of h, down output, S of the down product, |dh| bound) for
+    every row of x.  |dh| bounds |h_gpu - h| element by element from the
+    products' error bound (gemm_error_bound) through SiLU's Lipschitz
+    constant, plus the GPU's fp32 evaluation error and the fp32 rounding of h."""
+    qx, dx, sx = oq8.quantize_rows(x)
+    fg, fu, fd = q4k_blocks.decode(gate), q4k_blocks.decode(up), q4k_blocks.decode(down)
+    g = ogemm.gemm_blockwise(fg, qx, dx, sx)
+    u = ogemm.gemm_blockwise(fu, qx, dx, sx)
+    dg = gemm_error_bound(fg, qx, dx, sx)
+    du = gemm_error_bound(fu, qx, dx, sx)
+    h = osw.silu_mul_f64(g, u)
+    silu = osw.silu_mul_f64(g, np.ones_like(u))
+    dh = SILU_LIP * dg * (np.abs(u) + du) + np.abs(silu) * du + (EVAL_REL + 2 * U32) * (np.abs(h) + 1e-30)
+    h32 = h.astype(np.float32)
+    qa, da_bits, ssum = oq8.quantize_rows(h32)
+    y = ogemm.gemm_blockwise(fd, qa, da_bits, ssum)
+    s = ogemm.abs_scale(fd, qa, da_bits)
+    return h32, (qa, da_bits, ssum), y, s, dh
+
+
+def chain_accept(h32, q8_or, dh, qa_gpu, da_gpu):
+    """Every difference between the GPU's operand and the oracle's q8 of h must
+    be one the stated bounds allow.  Per 32-element block with oracle amax A
+    and inverse inv = 127/A, an error dh_k in h moves the pre-rounding value
+    v_k = h_k * inv by at most eta_k = inv (dh_k + |h_k| max_j dh_j / A) (the
+    second term: amax, hence inv, moves too) plus fp32 rounding; the GPU code
+    must be a correct rounding of some value within eta_k of v_k, and its d_a
+    the f16 rounding of some amax within max_j dh_j of A."""
+    qa, da_bits, _ = q8_or
+    m, k = h32.shape
+    hb = h32.astype(np.float64).reshape(m, k // 32, 32)
+    amax = np.abs(hb).max(axis=2)
+    dmax = dh.reshape(m, k // 32, 32).max(axis=2)
+    inv = 127.0 / np.maximum(amax - dmax, 1e-30)
+    v = hb * (127.0 / amax)[:, :, None]
+    eta = inv[:, :, None] * (dh.reshape(m, k // 32, 32) + np.abs(hb) * (dmax / amax)[:, :, None]) + 4 * 127 * U32
+    qg = qa_gpu.astype(np.float64).reshape(m, k // 32, 32)
+    bad = np.abs(qg - v) > 0.5 + eta
+    assert not bad.any(), f"{int(bad.sum())} GPU codes not explained by the bounds"
+    d_or = da_bits.view(np.float16).astype(np.float64)
+    d_lo = ((amax - dmax) / 127.0).astype(np.float32).astype(np.float16).astype(np.float64)
+    d_hi = ((amax + dmax) / 127.0).astype(np.float32).astype(np.float16).astype(np.float64)
+    da_g = da_gpu.astype(np.float64)
+    assert np.all((da_g >= d_lo) & (da_g <= d_hi)), "d_a outside the rounding of the allowed amax"
+    flips = int((qg.reshape(m, k) != qa).sum())
+    return flips, int((da_g != d_or).sum())
+
+
+def check_chain(down, x_rows, y_gpu, qa_gpu, da_gpu, chain, out, what):
+    """y_gpu (the down output of those rows) against the oracle chain."""
+    h32, q8_or, y_or, s_or, dh = chain
+    flips, dflips = chain_accept(h32, q8_or, dh, qa_gpu, da_gpu)
+    w = np.abs(q4k_blocks.dequantize(q4k_blocks.decode(down)))
+    qa, da_bits, _ = q8_or
+    a_or = oq8.dequantize_rows(qa, da_bits)
+    m, k = qa.shape
+    a_g = (qa_gpu.astype(np.float64).reshape(m, k // 32, 32) * da_gpu.astype(np.float64)[:, :, None]).reshape(m, k)
+    step = np.abs(a_g - a_or) @ w.T          # exact effect bound of the allowed code / scale steps
+    s_g = np.abs(a_g) @ w.T
+    tol = 1e-4 * np.maximum(s_or, s_g) + step
+    if out == "bf16":
+        tol = tol * (1.0 + BF16_U) + BF16_U * np.abs(y_or)
+    err = np.abs(y_gpu - y_or)
+    assert np.all(err <= tol), f"{what}: {int((err > tol).sum())} outside; worst {float((err / tol).max()):.3g}"
+    return flips, dflips
+
+
 def _case(n, k, m, seed):
     gate = inputs.q4k_blocks(n, k, seed, 11)
     up = inputs.q4k_blocks(n, k, seed, 12)
@@ -111,6 +210,24 @@ def test_swiglu_operand_bits_and_down_projection(q4k, n, k, m):
     want = ogemm.gemm_blockwise(fields, qa, da_bits, ssum)
     scale = ogemm.abs_scale(fields, qa, da_bits)
     assert_close(y.cpu().double().numpy(), want, scale, "f32", "down projection")
+
+
+@pytest.mark.parametrize("n,k,m", [(512, 1024, 200), (256, 512, 1), (1024, 768, 130)])
+def test_swiglu_chain_from_x_alone(q4k, n, k, m):
+    """x -> gate/up -> SiLU(g)*u -> q8 -> down on the GPU (fused pair GEMM
+    with the SiLU epilogue, then the down GEMM from its operand), against the
+    oracle chain computed from x alone with the plain fp64 SiLU."""
+    gate, up, x = _case(n, k, m, 300 + m)
+    down = inputs.q4k_blocks(256, n, 300 + m, 13)
+    packed = q4k.q4k_pack_swiglu_weights(to_dev(gate), to_dev(up), n, k)
+    pd = q4k.q4k_pack_weights(to_dev(down), 256, n)
+    h_ws = q4k.q4k_gemm_swiglu(packed, n, k, to_dev(x))
+    y = q4k.q4k_gemm_quantized(pd, 256, n, h_ws, m, "f32")
+    torch.cuda.synchronize()
+    xq, da, _ = _operand(h_ws.cpu().numpy(), m, n)
+    chain = chain_oracle(gate, up, down, x)
+    flips, _ = check_chain(down, x, y.cpu().double().numpy(), xq[:m], da[:m], chain, "f32", f"chain {n}x{k} m={m}")
+    assert flips <= max(4, m * n // 1000)   # rounding straddles are rare
 
 
 def test_swiglu_q8_input_matches_f32_input(q4k):
@@ -174,4 +291,9 @@ def test_swiglu_ffn_size_sampled(q4k):
     fields = q4k_blocks.decode(down)
     want = ogemm.gemm_blockwise(fields, qa[srows], da_bits[srows], ssum[srows])
     scale = ogemm.abs_scale(fields, qa[srows], da_bits[srows])
-    assert_close(y.float().cpu().double().numpy()[srows], want, scale, "bf16", "down projection")
+    yb = y.float().cpu().double().numpy()[srows]
+    assert_close(yb, want, scale, "bf16", "down projection")
+    # the same rows through the oracle chain from x alone
+    xq, da, _ = _operand(h_ws.cpu().numpy(), m, n)
+    chain = chain_oracle(gate, up, down, x[srows])
+    check_chain(down, x[srows], yb, xq[srows], da[srows], chain, "bf16", "FFN chain, sampled rows")

@@ -269,3 +269,94 @@ def test_degenerate_cases():
     fm = dict(fields, m=np.zeros_like(fields["m"]))
     ym = gemm.gemm_blockwise(fm, qa, da_bits, ssum)
     assert np.allclose(ym, gemm.gemm_dense(fm, qa, da_bits), rtol=1e-12, atol=1e-300)
+
+
+# ------------------------------------------------------- error scale S ----
+
+def _load_abs_scale_golden():
+    g = {}
+    with open(os.path.join(GOLDEN, "abs_scale_worked.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *vals = line.split()
+            g[key] = vals
+    return g
+
+
+def _sparse(tokens, k, dtype):
+    v = np.zeros(k, dtype=dtype)
+    for tok in tokens:
+        i, val = tok.split(":")
+        v[int(i)] = float(val)
+    return v
+
+
+def test_abs_scale_worked_token():
+    """S and y for one hand-worked token against the hand-worked block: the
+    scale of every acceptance bound is pinned to a value worked out by hand."""
+    blk, _ = _golden_block()
+    g = _load_abs_scale_golden()
+    fields = q4k_blocks.decode(blk)
+    x = _sparse(g["x"], 256, np.float32)[None, :]
+    qa, da_bits, ssum = q8.quantize_rows(x)
+    assert np.array_equal(qa[0], _sparse(g["qa"], 256, np.int64).astype(np.int8))
+    assert [int(v) for v in da_bits[0]] == [int(v, 16) for v in g["da_bits"]]
+    assert [int(v) for v in ssum[0]] == [int(v) for v in g["ssum"]]
+    w = q4k_blocks.dequantize(fields)
+    for tok in g["w"]:
+        i, v = tok.split(":")
+        assert w[0, int(i)] == float(v)
+    s = gemm.abs_scale(fields, qa, da_bits)
+    assert s.shape == (1, 1) and s[0, 0] == float(g["S"][0])
+    y = gemm.gemm_blockwise(fields, qa, da_bits, ssum)
+    assert y[0, 0] == float(g["y"][0])
+    assert gemm.gemm_dense(fields, qa, da_bits)[0, 0] == float(g["y"][0])
+
+
+def test_abs_scale_explicit_loops():
+    """S[t,o] = sum_k |w[o,k]| * |a[t,k]| by explicit loops over t, o, k, with
+    w and a formed element by element from the fields (w = d*sc*q - dmin*m,
+    a = d_a*qa): catches a dropped absolute value, a transposed operand or a
+    wrong sign of the min term in the vectorised form."""
+    rng = np.random.default_rng(17)
+    m, n, k = 3, 4, 512
+    blocks, x = _random_case(m, n, k, 17)
+    x = x * rng.choice([-1.0, 1.0], size=x.shape).astype(np.float32)
+    fields = q4k_blocks.decode(blocks)
+    qa, da_bits, _ = q8.quantize_rows(x)
+    d = q4k_blocks.f16_bits_to_f64(fields["d_bits"])
+    dmin = q4k_blocks.f16_bits_to_f64(fields["dmin_bits"])
+    da = q8.f16_bits_to_f64(da_bits)
+    got = gemm.abs_scale(fields, qa, da_bits)
+    for t in range(m):
+        for o in range(n):
+            acc = 0.0
+            for kk in range(k):
+                sb, c = kk // 256, kk // 32
+                w = float(d[o, sb]) * int(fields["sc"][o, c]) * int(fields["q"][o, kk]) \
+                    - float(dmin[o, sb]) * int(fields["m"][o, c])
+                a = float(da[t, c]) * int(qa[t, kk])
+                acc += abs(w * a)
+            assert abs(got[t, o] - acc) <= 1e-12 * acc
+
+
+def test_abs_scale_invariants():
+    """S >= |y| (triangle inequality), with equality when every product has one
+    sign: dmin*m = 0 and x >= 0 make every w*a >= 0, so S = y."""
+    blocks, x = _random_case(5, 6, 768, 23)
+    fields = q4k_blocks.decode(blocks)
+    qa, da_bits, ssum = q8.quantize_rows(x)
+    s = gemm.abs_scale(fields, qa, da_bits)
+    y = gemm.gemm_blockwise(fields, qa, da_bits, ssum)
+    assert np.all(s >= np.abs(y) * (1 - 1e-12))
+    assert np.any(s > 1.01 * np.abs(y))   # random signs: strict somewhere
+    f0 = dict(fields, m=np.zeros_like(fields["m"]))
+    qp, dp, sp = q8.quantize_rows(np.abs(x))
+    s0 = gemm.abs_scale(f0, qp, dp)
+    y0 = gemm.gemm_blockwise(f0, qp, dp, sp)
+    assert np.allclose(s0, y0, rtol=1e-12, atol=0)
+    # S scales with the activations' d_a exactly: doubling x doubles every d_a
+    qa2, da2, _ = q8.quantize_rows(2 * x)
+    assert np.array_equal(qa2, qa)
+    assert np.array_equal(gemm.abs_scale(fields, qa2, da2), 2 * s)

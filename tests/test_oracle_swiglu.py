@@ -84,3 +84,18 @@ def test_silu_limits():
         assert abs(got - want) <= 5e-7 * abs(want)
     # the value at g = 1: 1 / (1 + 1/e)
     assert abs(float(sw.silu_mul(np.float32(1.0), np.float32(1.0))) - 1.0 / (1.0 + math.exp(-1.0))) <= 2e-7
+
+
+def test_silu_mul_f64_definition_values():
+    """The fp64 form the FFN chain test takes as the definition: SiLU(0) = 0,
+    SiLU(1) = 1/(1 + 1/e), SiLU(g) - SiLU(-g) = g, SiLU(g) -> g for large g and
+    -> 0 for very negative g, and linearity in u."""
+    one = np.ones(1)
+    assert sw.silu_mul_f64(np.zeros(1), one)[0] == 0.0
+    assert abs(sw.silu_mul_f64(one, one)[0] - 1.0 / (1.0 + math.exp(-1.0))) <= 1e-16
+    g = np.linspace(-30.0, 30.0, 6001)
+    u = np.ones_like(g)
+    assert np.all(np.abs(sw.silu_mul_f64(g, u) - sw.silu_mul_f64(-g, u) - g) <= 1e-14 * (1.0 + np.abs(g)))
+    assert sw.silu_mul_f64(np.array([60.0]), one)[0] == 60.0
+    assert 0.0 > sw.silu_mul_f64(np.array([-60.0]), one)[0] > -1e-24
+    assert sw.silu_mul_f64(np.array([2.0]), np.array([-3.0]))[0] == -3.0 * sw.silu_mul_f64(np.array([2.0]), one)[0]
