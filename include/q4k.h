@@ -252,9 +252,11 @@ q4k_status q6k_gemm(const void* packed_w, int64_t n, int64_t k,
  *   Limit: q4k_gemm_workspace_bytes(m, n, k, act) must not exceed
  *   Q4K_STATIC_WORKSPACE_BYTES (64 MiB: e.g. m = 2048 tokens at k = 11008);
  *   larger problems return Q4K_ERR_WORKSPACE before anything is launched.
- *   Set-up: the first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress, with that device current); make that
- *   first call before any stream capture on the device.
+ *   Set-up: every call looks up the array's address in the current
+ *   context (cudaGetSymbolAddress, with the device current; nothing is
+ *   cached, so a reset device or another context never sees a stale
+ *   address).  The first lookup in a context loads the library's device code
+ *   into it: make the first call on each device before any stream capture.
  *   Sharing: all calls on one device use the same array and leave the last
  *   call's contents in it.  Calls that overlap in time on one device (other
  *   streams, other host threads) race on it; the caller must order them.

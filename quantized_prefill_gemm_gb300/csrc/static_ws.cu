@@ -10,15 +10,14 @@
 // any other allocating routine.
 //
 // The array lives for as long as the library stays loaded, one copy per
-// device context.  Every call on a device uses the same copy, so two calls
-// that overlap in time on one device (different streams, or different host
-// threads) race on it and corrupt each other's results: the caller must
-// order them.  Nothing in the array needs to start at zero: the
+// device context (each device's primary context, for runtime-API callers).
+// Every call in a context uses the same copy, so two calls that overlap in
+// time on one device (different streams, or different host threads) race on
+// it and corrupt each other's results: the caller must order them.  Nothing in the array needs to start at zero: the
 // quantization step of each call rewrites every byte the GEMM step reads.
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/q4k.h"
 
@@ -26,34 +25,28 @@ namespace q4k {
 namespace {
 
 constexpr size_t kStaticWsBytes = Q4K_STATIC_WORKSPACE_BYTES;
-constexpr int kMaxDevices = 64;
 
 // The scratch array.  Host code must not use this name as a device address;
-// the address comes from cudaGetSymbolAddress (per device, that device
-// current) in static_ws_address below.
+// the address comes from cudaGetSymbolAddress in static_ws_address below.
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
 
-std::mutex g_ws_mu;
-void* g_ws_ptr[kMaxDevices] = {};
-
-// Set-up on the first call for each device: look up the array's device
-// address in the current device's context.  Later calls reuse it.
+// The array's address in the current context, looked up on every call (the
+// lookup allocates nothing).  A cached address could belong to a context that
+// was since destroyed (cudaDeviceReset) or to another context on the same
+// device (driver-API contexts), so none is kept.  The first lookup in a
+// context loads this library's device code into it; that first call should
+// therefore come before any stream capture.
 q4k_status static_ws_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return Q4K_ERR_UNSUPPORTED_DEVICE;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return Q4K_ERR_CUDA;
     if (major != 10 || minor != 3) return Q4K_ERR_UNSUPPORTED_DEVICE;   // the array exists in sm_103a code only
-    std::lock_guard<std::mutex> lock(g_ws_mu);
-    if (!g_ws_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return Q4K_ERR_CUDA;
-        g_ws_ptr[dev] = ptr;
-    }
-    *out = g_ws_ptr[dev];
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return Q4K_ERR_CUDA;
+    *out = ptr;
     return Q4K_OK;
 }
 

@@ -45,24 +45,24 @@ def _case(q4k, n, k, m, kind, seed, act, out):
 
 
 @pytest.mark.gpu
-def test_two_calls_match_q4k_gemm(q4k):
-    """Two calls in a row with different shapes, activation forms and output
-    types: the second call reuses the array the first one left filled."""
-    calls = [
-        # n, k, m, kind, seed, act, out
-        (256, 1024, 300, "normal", 11, "f32", "f32"),
-        (384, 512, 130, "outlier", 12, "q8", "bf16"),
-    ]
+@pytest.mark.parametrize("calls", [
+    # n, k, m, kind, seed, act, out: two calls in a row, the second reusing the
+    # array the first left filled
+    [(256, 1024, 300, "normal", 11, "f32", "f32"), (384, 512, 130, "outlier", 12, "q8", "bf16")],
+    # small-M paths: m <= 4 with fp32 input quantizes in the product kernel (no
+    # workspace); 4 < m <= 16 with fp32 input stages the q8 rows in the array
+    [(256, 512, 3, "normal", 14, "f32", "f32"), (384, 1024, 9, "normal", 15, "f32", "bf16")],
+])
+def test_two_calls_match_q4k_gemm(q4k, calls):
+    """Same kernels as q4k_gemm on the same inputs: the output is identical bit
+    for bit, and within the test bound of the oracle."""
     for n, k, m, kind, seed, act, out in calls:
         blocks, x, ref, y = _case(q4k, n, k, m, kind, seed, act, out)
         torch.cuda.synchronize()
-        yr = ref.float().cpu().double().numpy()
+        assert torch.equal(y, ref), f"static vs q4k_gemm {n}x{k} m={m}: not bit-identical"
         ys = y.float().cpu().double().numpy()
         assert np.isfinite(ys).all()
-        rows = np.arange(m)
-        want, scale = oracle_rows(blocks, x, rows)
-        # same kernels as q4k_gemm: agreement within the test bound, and both within it of the oracle
-        assert_close(ys, yr, scale, out, f"static vs q4k_gemm {n}x{k} m={m}")
+        want, scale = oracle_rows(blocks, x, np.arange(m))
         assert_close(ys, want, scale, out, f"static vs oracle {n}x{k} m={m}")
 
 
