@@ -631,21 +631,17 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
             P[j] = 0.0f;
         }
         // d_a straight from global memory (this thread's token, two chunks per
-        // accumulator group), loaded two groups ahead so that its latency (the L2
-        // under the GEMM's own load) is hidden
+        // accumulator group), loaded kDaAhead groups ahead so that its latency
+        // (the L2 under the GEMM's own load) is hidden: dq holds the next groups'
+        // values in order, two per group
+        constexpr int kDaAhead = 3;
         const int c_end = L::kCh * (w.kbase + w.n_st);
         const float* dap = p.da + static_cast<int64_t>(mt) * p.kc * 128 + row;   // + 128 * chunk
-        float da_n0 = 0.0f, da_n1 = 0.0f, da_m0 = 0.0f, da_m1 = 0.0f;
+        float dq[2 * kDaAhead];
         {
             const int c0 = L::kCh * max(w.kbase, 0);
-            if (c0 < c_end) {
-                da_n0 = __ldg(dap + 128 * c0);
-                da_n1 = __ldg(dap + 128 * (c0 + 1));
-            }
-            if (c0 + 2 < c_end) {
-                da_m0 = __ldg(dap + 128 * (c0 + 2));
-                da_m1 = __ldg(dap + 128 * (c0 + 3));
-            }
+#pragma unroll
+            for (int i = 0; i < 2 * kDaAhead; ++i) dq[i] = c0 + i < c_end ? __ldg(dap + 128 * (c0 + i)) : 0.0f;
         }
         for (int st = 0; st < w.n_st; ++st) {
             const int kb = st + w.kbase;
@@ -675,12 +671,12 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
 #pragma unroll 1
                 for (int j = 0; j < L::kCh / 2; ++j) {   // one accumulator group per two chunks
                     const int c = L::kCh * kb + 2 * j;    // its first chunk
-                    const float da0 = da_n0, da1 = da_n1;
-                    da_n0 = da_m0;
-                    da_n1 = da_m1;
-                    if (c + 4 < c_end) {
-                        da_m0 = __ldg(dap + 128 * (c + 4));
-                        da_m1 = __ldg(dap + 128 * (c + 5));
+                    const float da0 = dq[0], da1 = dq[1];
+#pragma unroll
+                    for (int i = 0; i + 2 < 2 * kDaAhead; ++i) dq[i] = dq[i + 2];
+                    if (c + 2 * kDaAhead < c_end) {
+                        dq[2 * kDaAhead - 2] = __ldg(dap + 128 * (c + 2 * kDaAhead));
+                        dq[2 * kDaAhead - 1] = __ldg(dap + 128 * (c + 2 * kDaAhead + 1));
                     }
                     if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiAccFull)) {
                         ok = false;
