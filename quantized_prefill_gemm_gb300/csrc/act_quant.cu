@@ -20,6 +20,7 @@
 #include "q4k_internal.h"
 #include "q4k_layout.h"
 #include "q4k_ptx.cuh"
+#include "q8_rule.cuh"
 
 namespace q4k {
 namespace {
@@ -42,24 +43,20 @@ __device__ __forceinline__ LaneQ8 quantize_lane(float4 v) {
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1, 8));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2, 8));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4, 8));
-    const bool live = amax >= 0x1p-120f;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __fdiv_rn(127.0f, amax);
+    const Q8Scale sc = q8_scale(amax);
     LaneQ8 r;
     const float xs[4] = {v.x, v.y, v.z, v.w};
     int s = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int q = __float2int_rn(__fmul_rn(xs[i], inv));
-        q = max(-127, min(127, q));
-        r.q[i] = live ? q : 0;
+        r.q[i] = q8_code(xs[i], sc);
         s += r.q[i];
     }
     s += __shfl_xor_sync(kFull, s, 1, 8);
     s += __shfl_xor_sync(kFull, s, 2, 8);
     s += __shfl_xor_sync(kFull, s, 4, 8);
     r.ssum = s;
-    r.da = __float2half_rn(live ? d : 0.0f);
+    r.da = sc.da;
     return r;
 }
 
@@ -85,18 +82,15 @@ __device__ __forceinline__ BlockQ8 quantize_block(const float* __restrict__ src)
     float amax = fabsf(v[0]);
 #pragma unroll
     for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const bool live = amax >= 0x1p-120f;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __fdiv_rn(127.0f, amax);
+    const Q8Scale sc = q8_scale(amax);
     BlockQ8 b;
     b.ssum = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const int q = max(-127, min(127, __float2int_rn(__fmul_rn(v[i], inv))));
-        b.q[i] = live ? q : 0;
+        b.q[i] = q8_code(v[i], sc);
         b.ssum += b.q[i];
     }
-    b.da = __float2half_rn(live ? d : 0.0f);
+    b.da = sc.da;
     return b;
 }
 

@@ -46,6 +46,7 @@
 #include "q4k_layout.h"
 #include "q4k_ptx.cuh"
 #include "q4k_unpack.cuh"
+#include "q8_rule.cuh"
 
 namespace q4k {
 namespace {
@@ -568,17 +569,13 @@ __device__ __forceinline__ void swiglu_store(const GemmParams& p, int64_t t, int
     float amax = fabsf(h[0]);
 #pragma unroll
     for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-    const bool live = amax >= 0x1p-120f;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __fdiv_rn(127.0f, amax);
+    const Q8Scale sc = q8_scale(amax);
     int ssum = 0;
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-        int q0 = max(-127, min(127, __float2int_rn(__fmul_rn(h[i], inv))));
-        int q1 = max(-127, min(127, __float2int_rn(__fmul_rn(h[i + 1], inv))));
-        q0 = live ? q0 : 0;
-        q1 = live ? q1 : 0;
+        const int q0 = q8_code(h[i], sc);
+        const int q1 = q8_code(h[i + 1], sc);
         ssum += q0 + q1;
         const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
         w[i >> 1] = *reinterpret_cast<const uint32_t*>(&pr);
@@ -587,7 +584,7 @@ __device__ __forceinline__ void swiglu_store(const GemmParams& p, int64_t t, int
     uint4* dst = reinterpret_cast<uint4*>(p.hq + t * kd + 32 * c);
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    const __half da = __float2half_rn(live ? d : 0.0f);
+    const __half da = sc.da;
     p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = __half2float(da);
     const float e = __fmul_rn(__half2float(da), static_cast<float>(ssum));   // exact: 11 x <= 13 bits
     const __nv_bfloat16 hi = __float2bfloat16_rn(e);
@@ -914,13 +911,9 @@ __global__ void __launch_bounds__(256) split_fixup_swiglu_kernel(const GemmParam
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     amax = __shfl_sync(kFull, amax, 0);
-    const bool live = amax >= 0x1p-120f;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __fdiv_rn(127.0f, amax);
-    int q0 = max(-127, min(127, __float2int_rn(__fmul_rn(h0, inv))));
-    int q1 = max(-127, min(127, __float2int_rn(__fmul_rn(h1, inv))));
-    q0 = (live && gl) ? q0 : 0;
-    q1 = (live && gl) ? q1 : 0;
+    const Q8Scale sc = q8_scale(amax);
+    const int q0 = gl ? q8_code(h0, sc) : 0;
+    const int q1 = gl ? q8_code(h1, sc) : 0;
     int ssum = q0 + q1;
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ssum += __shfl_xor_sync(kFull, ssum, o);
@@ -930,7 +923,7 @@ __global__ void __launch_bounds__(256) split_fixup_swiglu_kernel(const GemmParam
         *reinterpret_cast<__half2*>(p.hq + t * kd + 32 * c + 2 * lane) = pr;
     }
     if (lane == 0) {
-        const __half da = __float2half_rn(live ? d : 0.0f);
+        const __half da = sc.da;
         p.hda[((t >> 7) * p.hkc + c) * 128 + (t & 127)] = __half2float(da);
         const float ev = __fmul_rn(__half2float(da), static_cast<float>(ssum));
         const __nv_bfloat16 hi = __float2bfloat16_rn(ev);

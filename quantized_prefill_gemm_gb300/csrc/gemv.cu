@@ -37,6 +37,7 @@
 
 #include "q4k_internal.h"
 #include "q4k_ptx.cuh"
+#include "q8_rule.cuh"
 #include "q4k_unpack.cuh"
 
 namespace q4k {
@@ -101,16 +102,12 @@ __device__ __forceinline__ void quantize_to_stage(const float* __restrict__ x, u
 #pragma unroll
     for (int i = 1; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, 1));
-    const bool live = amax >= 0x1p-120f;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __fdiv_rn(127.0f, amax);
+    const Q8Scale sc = q8_scale(amax);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     int s = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        int q = __float2int_rn(__fmul_rn(v[i], inv));
-        q = max(-127, min(127, q));
-        q = live ? q : 0;
+        const int q = q8_code(v[i], sc);
         s += q;
         w[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
     }
@@ -118,7 +115,7 @@ __device__ __forceinline__ void quantize_to_stage(const float* __restrict__ x, u
     st.qa[t][hl] = make_int4(static_cast<int>(w[0]), static_cast<int>(w[1]), static_cast<int>(w[2]),
                              static_cast<int>(w[3]));
     if ((hl & 1) == 0) {
-        reinterpret_cast<uint16_t*>(&st.da[t])[hl >> 1] = __half_as_ushort(__float2half_rn(live ? d : 0.0f));
+        reinterpret_cast<uint16_t*>(&st.da[t])[hl >> 1] = __half_as_ushort(sc.da);
         reinterpret_cast<int16_t*>(&st.ss[t])[hl >> 1] = static_cast<int16_t>(s);
     }
 }
@@ -289,21 +286,18 @@ __device__ __forceinline__ void quantize_block_to(const float* __restrict__ src,
     float amax = fabsf(v[0]);
 #pragma unroll
     for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const bool live = amax >= 0x1p-120f;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __fdiv_rn(127.0f, amax);
+    const Q8Scale sc = q8_scale(amax);
     uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     int s = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        int q = max(-127, min(127, __float2int_rn(__fmul_rn(v[i], inv))));
-        q = live ? q : 0;
+        const int q = q8_code(v[i], sc);
         s += q;
         w[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
     }
     reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
     reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    *da = __half_as_ushort(__float2half_rn(live ? d : 0.0f));
+    *da = __half_as_ushort(sc.da);
     *ss = static_cast<int16_t>(s);
 }
 

@@ -43,6 +43,7 @@ SIGNATURES = {
     "q4k_device_error_word": (_c_uint, [_c_int]),
     "q4k_device_status": (_c_int, [_c_int]),
     "q4k_selftest_wait_timeout": (_c_int, [_c_i64, _c_ptr]),
+    "q4k_peak_mma_s8": (_c_int, [_c_i64, _c_i64, _c_ptr, _c_ptr]),
     "q4k_gemm_debug_chunk_acc": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_i64,
                                           _c_ptr, _c_ptr]),
     "q4k_swiglu_packed_bytes": (_c_size, [_c_i64, _c_i64]),
@@ -282,7 +283,10 @@ def q6k_pack_weights(blocks: torch.Tensor, n: int, k: int, packed=None, stream=N
 
 def q6k_gemm(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, out_dtype="f32", da=None, ssum=None,
              y=None, workspace=None, stream=None) -> torch.Tensor:
-    """Y[m][n] = x @ W^T for Q6_K weights, 1 <= m <= 16 tokens."""
+    """Y[m][n] = x @ W^T for Q6_K weights (q6k_pack_weights), any m >= 1.
+
+    Up to 16 tokens whose activations fit the small-M kernel's shared memory
+    take the CUDA-core product; larger batches take the tensor-core GEMM."""
     m, kx, ldx = _row_major(x, "x")
     if kx != k:
         raise ValueError("x has the wrong number of columns")
@@ -341,6 +345,12 @@ def q6k_gemm_debug_chunk_acc(packed, n, k, workspace, m, stream=None):
         _dev(packed, "packed"), n, k, _dev(workspace, "workspace"), workspace.numel(), m, _dev(y, "y"), n,
         _dev(acc, "acc"), _stream(stream)))
     return y, acc
+
+
+def q4k_peak_mma_s8(blocks: int, iters: int, sink: torch.Tensor, stream=None) -> None:
+    """Launch the INT8 tensor-peak kernel (diagnostics): blocks x 8 warps x iters x 8
+    mma.sync m16n8k32 s8, 8192 integer ops each; the caller times it."""
+    _check("q4k_peak_mma_s8", LIB.q4k_peak_mma_s8(blocks, iters, _dev(sink, "sink", torch.int32), _stream(stream)))
 
 
 def q4k_device_error_word(reset: bool = False) -> int:
