@@ -15,6 +15,11 @@ three GEMMs with separate fp32 inputs).
 path, bound by reading 3.64 GB of packed weights), captured in a CUDA graph
 so that the timed region holds no host launch overhead.
 
+--workload tiny is the smallest configuration (256 x 512 weights, 64 tokens
+given pre-quantized as q8 blocks); --workload peak_s8 only measures the
+GPU's dense INT8 tensor rate (mma.sync s8), the denominator of the literal
+INT8 roofline fraction every prefill line also reports.
+
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
 Multi-GPU (torchrun): every rank runs its own replica of the workload (no data
 exchange); value = all ranks' tokens / max step time over ranks.
@@ -45,10 +50,15 @@ WORKLOADS = {
     "ffn": (2048, [(11008, 4096), (11008, 4096), (4096, 11008)], "bf16",
             "7B FFN linears gate/up 11008x4096 + down 4096x11008 Q4_K, 2048 tokens, fused q8, bf16 out"),
     "qproj2630": (2630, [(4096, 4096)], "bf16", "7B q-proj 4096x4096 Q4_K, 2630 tokens (outlier channels), fused q8, bf16 out"),
+    "attn_proj": (2048, [(4096, 4096)] * 4, "bf16",
+                  "7B attention projections q, k, v, o 4096x4096 Q4_K of one layer, 2048 tokens, fused q8, bf16 out"),
     "down_q6k": (2048, [(4096, 11008)] * 8, "bf16",
                  "7B down projection 4096x11008 with Q6_K weights (as Q4_K_M models store it), 2048 tokens, "
                  "8 distinct matrices and inputs per step, fused q8, bf16 out (tensor-core path)"),
     "qproj512": (512, [(4096, 4096)], "f32", "7B q-proj 4096x4096 Q4_K, 512 tokens, fused q8, fp32 out"),
+    "tiny": (64, [(256, 512)], "f32",
+             "tiny Q4_K x q8 GEMM 256x512 (2 super-blocks per row), 64 tokens given as the q8 SoA of "
+             "q8_quantize_rows (q4k_gemm's q8 input path), fp32 out"),
     "ffn_swiglu": (2048, [(22016, 4096), (4096, 11008)], "bf16",
                    "7B FFN with the SiLU(gate)*up epilogue: gate+up 11008x4096 as one pair GEMM whose epilogue "
                    "writes the q8 input of down 4096x11008, Q4_K, 2048 tokens, fused q8 of x, bf16 out"),
@@ -144,6 +154,60 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def measure_s8_peak(torch, q4k, dev, sms):
+    """Dense INT8 tensor rate of this GPU in T-ops/s: the library's mma.sync
+    s8 kernel (register operands only) on 4 CTAs per SM, best of 3 timed
+    launches after one warm-up."""
+    blocks, iters = 4 * sms, 20000
+    sink = torch.zeros(blocks, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    q4k.q4k_peak_mma_s8(blocks, 200, sink, stream=stream)
+    best = None
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q4k.q4k_peak_mma_s8(blocks, iters, sink, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    ops = blocks * 8 * iters * 8 * 8192.0
+    return ops / (best * 1e-3) / 1e12
+
+
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "traffic__q4k_gemm_kernel.txt")
+
+
+def gemm_traffic(mats, tokens, q6):
+    """DRAM bytes per GEMM launch, averaged over the step's launches, from the
+    per-shape ncu captures in profiles/ (lines "M N K bytes"), valid only for
+    the kernel build they were taken on ("digest" line = the build's source
+    digest).  Returns (bytes or None, note)."""
+    from quantized_prefill_gemm_gb300 import build as qbuild
+
+    if q6:
+        return None, "no per-shape capture of the Q6_K kernel"
+    if not os.path.exists(TRAFFIC_TABLE):
+        return None, "no traffic table"
+    digest, shapes = None, {}
+    with open(TRAFFIC_TABLE) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "digest":
+                digest = parts[1]
+            elif len(parts) == 4 and all(p.isdigit() for p in parts):
+                shapes[tuple(int(p) for p in parts[:3])] = int(parts[3])
+    if digest != qbuild._digest():
+        return None, "kernel changed since the ncu capture (digest mismatch)"
+    try:
+        vals = [shapes[(tokens, n, k)] for n, k in mats]
+    except KeyError as e:
+        return None, f"shape {e} not captured"
+    return sum(vals) / len(vals), f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch ({TRAFFIC_TABLE[len(ROOT) + 1:]})"
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 100 ms while running
     (a timed region shorter than nvidia-smi's start-up, such as a few decode
@@ -184,60 +248,95 @@ class ClockSampler:
                 "power_w_max": max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)}
 
 
-def cpu_baseline(workload, seconds=10.0):
-    """The oracle as it stands, on a bounded sample: 32 tokens through one
-    q-proj-shaped matrix (4096x4096), repeated until `seconds` have passed;
-    the time is scaled to the workload by its total weight count."""
-    import numpy as np
+ORACLE_SAMPLE = (4096, 4096, 32)   # n, k, tokens of one oracle sample
 
+
+def _oracle_sample(workload):
+    """Build one bounded sample of the workload for the oracle: 32 tokens
+    through one q-proj-shaped matrix (4096 x 4096) of the workload's weight
+    format.  Returns (run, scale): run() computes the sample once (q8
+    quantization + blockwise GEMM); scale = how many samples the workload's
+    step holds (weight count x tokens)."""
     from oracle import gemm as ogemm
     from oracle import q4k_blocks, q6k_blocks, q8 as oq8
     from quantized_prefill_gemm_gb300 import inputs
 
     tokens, mats, _, _ = WORKLOADS[workload]
-    n, k, t = 4096, 4096, 32
+    n, k, t = ORACLE_SAMPLE
+    if sum(nn * kk for nn, kk in mats) * tokens <= n * k * t and len(set(mats)) == 1:
+        (n, k), t = mats[0], tokens   # a workload smaller than the sample runs whole
     q6 = workload in ("decode_q6k", "down_q6k")
-    if q6:
-        fields = q6k_blocks.decode(inputs.q6k_blocks(n, k, 99))
-    else:
-        fields = q4k_blocks.decode(inputs.q4k_blocks(n, k, 99))
+    fields = (q6k_blocks if q6 else q4k_blocks).decode((inputs.q6k_blocks if q6 else inputs.q4k_blocks)(n, k, 99))
     x = inputs.activations(t, k, 99)
-    reps, t0 = 0, time.perf_counter()
-    while True:
+
+    def run():
         qa, da, ss = oq8.quantize_rows(x)
         if q6:
             q6k_blocks.gemm_blockwise(fields, qa, da)
         else:
             ogemm.gemm_blockwise(fields, qa, da, ss)
+
+    scale = sum(nn * kk for nn, kk in mats) / (n * k) * (tokens / t)
+    return run, scale, q6, (n, k, t)
+
+
+def _oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+
+        return max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(workload, seconds=10.0):
+    """The oracle as it stands, on a bounded sample repeated until `seconds`
+    have passed; the time is scaled to the workload's step (weights x tokens)."""
+    run, scale, q6, (n, k, t) = _oracle_sample(workload)
+    tokens = WORKLOADS[workload][0]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
     per = (time.perf_counter() - t0) / reps
-    scale = sum(nn * kk for nn, kk in mats) / (n * k)
-    step_s = per * scale * (tokens / t)
-    try:
-        from threadpoolctl import threadpool_info
-
-        cores = max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
-    except Exception:
-        cores = os.cpu_count()
-    return {"value": tokens / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{t} tokens x one 4096x4096 {'Q6_K' if q6 else 'Q4_K'} matrix (numpy fp64 oracle: q8 quantization + blockwise "
-                      f"GEMM), {reps} repeats in {time.perf_counter() - t0:.1f} s, scaled by weight count "
-                      f"({scale:.1f}x) and tokens ({tokens // t}x) to the workload"}, step_s
+    step_s = per * scale
+    return {"value": tokens / step_s, "unit": "tok/s", "cores": _oracle_cores(), "kind": "oracle",
+            "sample": f"{t} tokens x one {n}x{k} {'Q6_K' if q6 else 'Q4_K'} matrix (numpy fp64 oracle: q8 "
+                      f"quantization + blockwise GEMM), {reps} repeats in {time.perf_counter() - t0:.1f} s, "
+                      + (f"extrapolated x{scale:.0f} (weight count and tokens) to the workload's step" if scale > 1 else
+                         "the whole workload")}, step_s
 
 
 def run_reference(args, rank):
+    """The oracle as the reference arm.  Each step is one bounded sample of
+    the workload (32 tokens through one 4096 x 4096 matrix), W untimed and K
+    timed; the value is the workload's tok/s extrapolated from the timed
+    samples (the sample's share of the step's weights and tokens)."""
     if rank != 0:
         return
-    base, step_s = cpu_baseline(args.workload, seconds=max(5.0, min(30.0, 3.0 * (args.steps + args.warmup))))
+    run, scale, q6, (n, k, t) = _oracle_sample(args.workload)
     tokens, mats, _, desc = WORKLOADS[args.workload]
-    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    sample_s = (time.perf_counter() - t0) / args.steps
+    value = tokens / (sample_s * scale)
+    sample = (f"each step: {t} tokens x one {n}x{k} {'Q6_K' if q6 else 'Q4_K'} matrix (numpy fp64 oracle: q8 "
+              "quantization + blockwise GEMM)" + (f"; value extrapolated x{scale:.0f} to the workload's step" if scale > 1
+                                                else " = the whole workload"))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sample_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats)},
-            "cpu_baseline": base,
-            "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "extrapolated": scale > 1, "step_is": "one bounded sample (ms_per_step is the sample's own time)",
+            "workload_ms_per_step_extrapolated": sample_s * scale * 1e3,
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": _oracle_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -247,7 +346,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS) + ["peak_s8"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -273,6 +372,8 @@ def main():
 
         dist.init_process_group("nccl", device_id=dev)
 
+    if args.workload == "peak_s8":
+        return run_peak_s8(args, q4k, torch, dev, dist, world, rank, local)
     tokens, mats, out, desc = WORKLOADS[args.workload]
     sms = min(torch.cuda.get_device_properties(dev).multi_processor_count, 160)
     if args.workload == "ffn_swiglu":
@@ -292,6 +393,8 @@ def main():
         kind_i = "silu_mul" if (args.workload == "ffn" and i == 2) else kind
         xs.append(inputs.activations_torch(tokens, k, seed=replica_seed(rank), kind=kind_i, tag=i, device=dev))
         ys.append(torch.empty((tokens, n), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device=dev))
+    # the tiny configuration takes its activations as the q8 SoA (quantized once, outside the steps)
+    q8in = [q4k.q8_quantize_rows(x) for x in xs] if args.workload == "tiny" else None
     ws_bytes = max(q4k.q4k_act_workspace_bytes(tokens, k) for _, k in mats)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -306,7 +409,10 @@ def main():
                     events[i][0].record(stream)
                 q4k.q6k_gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws, stream=stream)
             else:
-                q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
+                if q8in is not None:   # the q8 SoA -> the GEMM's operand form
+                    q4k.q4k_act_from_q8(*q8in[i], workspace=ws, stream=stream)
+                else:
+                    q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
                 if events is not None:
                     events[i][0].record(stream)
                 q4k.q4k_gemm_quantized(packed[i], n, k, ws, tokens, out, y=ys[i], stream=stream)
@@ -325,6 +431,8 @@ def main():
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in mats]
     inst = args.steps - 1
     wb, xb, yb = step_footprint(tokens, mats, out, 210 if q6 else 144)
+    if q8in is not None:   # activations read as q8 blocks: 36 B per 32 values
+        xb = xb * 36 // (32 * 4)
     flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if wb + xb + yb < 2 * L2_BYTES else None)
     clocks = ClockSampler(local)
     torch.cuda.synchronize()
@@ -345,11 +453,15 @@ def main():
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     achieved = flops_step / (gemm_ms * 1e-3) / 1e12
-    # dram__bytes_read.sum + dram__bytes_write.sum of q4k_gemm_kernel per launch, averaged over the 224
-    # launches of one stack step (ncu capture of this kernel version, summarized under profiles/)
-    traffic = 48.77e6 if args.workload == "stack" else None
+    traffic, traffic_note = gemm_traffic(mats, tokens, q6)
+    s8_peak = measure_s8_peak(torch, q4k, dev, sms)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic, "traffic_unit": "bytes per launch",
+                "traffic": traffic, "traffic_unit": "bytes per launch", "traffic_source": traffic_note,
+                "frac_int8_literal": achieved / s8_peak,
+                "int8_literal": {"peak": s8_peak, "unit": "T-ops/s",
+                                 "source": "measured in this run: mma.sync m16n8k32 s8 on register operands, all SMs "
+                                           "(sm_103a has no integer tcgen05 MMA); the GEMM's algorithmic 2*M*N*K "
+                                           "integer ops over it, so the fraction exceeds 1"},
                 "kernel": "q4k_gemm_kernel" + ("<Q6_K>" if q6 else ""),
                 "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step); the GEMM issues "
                                "f16 tcgen05 MMAs, same rate class",
@@ -358,8 +470,11 @@ def main():
 
     e2e = None
     if not args.no_e2e and rank == 0:
-        e2e = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream,
-                      gemm=q4k.q6k_gemm if q6 else None)
+        if q8in is not None:
+            e2e = run_e2e_q8(q4k, torch, dev, packed, mats, tokens, out, q8in, ws, stream)
+        else:
+            e2e = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream,
+                          gemm=q4k.q6k_gemm if q6 else None)
 
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -375,8 +490,9 @@ def main():
             "effective_tops": eff_tops, "gemm_ms_per_step": gemm_ms,
             "roofline": roofline,
             "hbm": hbm_view(peaks, src, wb + xb + yb, ms_step,
-                            "algorithmic bytes per step (packed weights at {} B/256, fp32 X, Y at its dtype) / "
-                            "step time: distance from the HBM limit of a tensor-bound path".format(210 if q6 else 144)),
+                            "algorithmic bytes per step (packed weights at {} B/256, {} X, Y at its dtype) / "
+                            "step time: distance from the HBM limit of a tensor-bound path".format(
+                                210 if q6 else 144, "q8 SoA" if q8in is not None else "fp32")),
             "clocks": clk,
             "gpu_launches": sum(gemm_launches(tokens, n, k, sms) for n, k in mats) * args.steps}
     if e2e is not None:
@@ -641,6 +757,56 @@ def run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream, steps=3,
             "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ms, "steps": steps,
             "overlap": (f"copies batched per {group} projections" if group > 1 else "copies per projection")
                        + " on their own streams, two device buffer sets"}
+
+
+def run_e2e_q8(q4k, torch, dev, packed, mats, tokens, out, q8in, ws, stream, steps=20):
+    """e2e for a step whose activations arrive as the q8 SoA: each step copies
+    every projection's q8 codes, d_a and ssum from pinned host memory, calls
+    q4k_gemm with the q8 input and copies the result back."""
+    ydt = torch.bfloat16 if out == "bf16" else torch.float32
+    host = [tuple(t.cpu().pin_memory() for t in q) for q in q8in]
+    devb = [tuple(torch.empty_like(t) for t in q) for q in q8in]
+    ys = [torch.empty((tokens, n), dtype=ydt, device=dev) for n, _ in mats]
+    hys = [torch.empty((tokens, n), dtype=ydt, pin_memory=True) for n, _ in mats]
+
+    def step():
+        for i, (n, k) in enumerate(mats):
+            for d, h in zip(devb[i], host[i]):
+                d.copy_(h, non_blocking=True)
+            q, da, ss = devb[i]
+            q4k.q4k_gemm(packed[i], n, k, q, out_dtype=out, da=da, ssum=ss, y=ys[i], workspace=ws, stream=stream)
+            hys[i].copy_(ys[i], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(sum(t.numel() * t.element_size() for t in q) for q in q8in)
+    d2h = sum(tokens * n * (2 if out == "bf16" else 4) for n, _ in mats)
+    return {"value": tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps, "overlap": "none: copies and the call in order on one stream"}
+
+
+def run_peak_s8(args, q4k, torch, dev, dist, world, rank, local):
+    """Only the INT8 tensor rate (the denominator of frac_int8_literal)."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clocks = ClockSampler(local)
+    tops = measure_s8_peak(torch, q4k, dev, sms)
+    clk = clocks.stop()
+    tops = max_over_ranks(tops, dist, dev) if dist else tops
+    if rank == 0:
+        print(json.dumps({"metric": "dense INT8 tensor rate (mma.sync m16n8k32 s8, register operands)", "value": tops,
+                          "unit": "T-ops/s", "n_gpus": world, "steps": 3, "warmup": 1, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "s8 x s8 -> s32", "data": "synthetic",
+                          "config": {"workload": "peak_s8: 4 CTAs x 256 threads per SM, 20000 x 8 MMAs per warp"},
+                          "clocks": clk, "gpu_launches": 4}), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 def run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream):

@@ -281,6 +281,16 @@ q4k_status q4k_gemm_static_workspace(const void* packed_w, int64_t n, int64_t k,
  *                        and returns the status the host reads back: it must
  *                        be Q4K_ERR_TIMEOUT.  Exercises the bounded-wait path
  *                        without faulting or hanging the GPU.
+ * q4k_peak_mma_s8        diagnostics for the roofline, not part of the product:
+ *                        launches `blocks` CTAs of 256 threads whose warps
+ *                        each issue iters x 8 dense mma.sync m16n8k32 s8 x s8
+ *                        -> s32 on register operands and nothing else (sm_103a
+ *                        has no integer tcgen05 MMA, so this is the GPU's INT8
+ *                        tensor rate); sink (device, >= blocks ints) receives
+ *                        one checksum per CTA.  The caller times the launch:
+ *                        blocks * 8 * iters * 8 * 8192 integer ops.
+ *                        Asynchronous; INVALID_ARG outside 1 <= blocks <= 2^20,
+ *                        1 <= iters <= 2^24 or for a null sink.
  * q4k_gemm_debug_chunk_acc  q4k_gemm_quantized with fp32 output that also
  *                        writes every per-chunk accumulator J[t][o][c] =
  *                        sum_{k in chunk c} (sc*q)[o,k]*qa[t,k] (exact
@@ -296,6 +306,7 @@ q4k_status q4k_gemm_static_workspace(const void* packed_w, int64_t n, int64_t k,
 unsigned int q4k_device_error_word(int reset);
 q4k_status q4k_device_status(int reset);
 q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
+q4k_status q4k_peak_mma_s8(int64_t blocks, int64_t iters, int* sink, cudaStream_t stream);
 q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k,
                                     void* workspace, size_t workspace_bytes, int64_t m,
                                     float* y, int64_t ldy, float* chunk_acc, cudaStream_t stream);

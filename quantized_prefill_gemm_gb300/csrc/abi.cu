@@ -620,6 +620,15 @@ q4k_status q4k_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
     return q4k_device_status(1);
 }
 
+q4k_status q4k_peak_mma_s8(int64_t blocks, int64_t iters, int* sink, cudaStream_t stream) {
+    if (blocks < 1 || blocks > (int64_t(1) << 20) || iters < 1 || iters > (int64_t(1) << 24)) return Q4K_ERR_INVALID_ARG;
+    if (!sink) return Q4K_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    const q4k_status st = device_info(&dev);
+    if (st != Q4K_OK) return st;
+    return from_cuda(launch_peak_s8(blocks, iters, sink, stream));
+}
+
 q4k_status q4k_gemm_debug_chunk_acc(const void* packed_w, int64_t n, int64_t k, void* workspace,
                                     size_t workspace_bytes, int64_t m, float* y, int64_t ldy, float* chunk_acc,
                                     cudaStream_t stream) {

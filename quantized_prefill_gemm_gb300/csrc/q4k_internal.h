@@ -109,5 +109,7 @@ cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
 bool gemv_q6k_fits(int m, int64_t k);
 cudaError_t launch_gemv_q6k(const GemvParams& p, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned* err, uint64_t timeout_cycles, cudaStream_t s);
+// blocks x 256 threads, each warp iters x 8 mma.sync m16n8k32 s8 (peak.cu)
+cudaError_t launch_peak_s8(int64_t blocks, int64_t iters, int* sink, cudaStream_t s);
 
 }  // namespace q4k
