@@ -43,7 +43,8 @@ def _digest() -> str:
             h.update(f.encode())
             with open(path, "rb") as fh:
                 h.update(fh.read())
-    h.update(" ".join(ARCH + CFLAGS + SOURCES).encode())
+    # flags without the include paths, which are absolute and differ between checkouts
+    h.update(" ".join(ARCH + [c for c in CFLAGS if not c.startswith("-I")] + SOURCES).encode())
     return h.hexdigest()
 
 
