@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libq4k.so")
 STAMP = LIB_PATH + ".stamp"
 
-SOURCES = ["abi.cu", "act_quant.cu", "pack.cu", "gemm.cu", "gemv.cu", "static_ws.cu", "peak.cu"]
+SOURCES = ["abi.cu", "act_quant.cu", "pack.cu", "gemm.cu", "gemv.cu", "gemv_stream.cu", "static_ws.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I" + INCLUDE, "-I" + CSRC]

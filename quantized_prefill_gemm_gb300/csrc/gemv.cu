@@ -673,6 +673,9 @@ bool gemv_q6k_fits(int m, int64_t k) {
 }
 
 cudaError_t launch_gemv_q6k(const GemvParams& p, cudaStream_t s) {
+    bool launched = false;
+    const cudaError_t e = launch_gemv_stream(p, s, &launched);
+    if (e != cudaSuccess || launched) return e;
     if (p.xf) {   // in-kernel quantization: up to 4 tokens (the caller's limit)
         if (p.m <= 1) return launch_q6k_gemv_m<1, true>(p, s);
         if (p.m <= 2) return launch_q6k_gemv_m<2, true>(p, s);
@@ -687,6 +690,9 @@ cudaError_t launch_gemv_q6k(const GemvParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
+    bool launched = false;
+    const cudaError_t e = launch_gemv_stream(p, s, &launched);
+    if (e != cudaSuccess || launched) return e;
     if (!p.xf) return launch_gemv_q8(p, s);
     // in-kernel quantization is built for up to 4 tokens (the caller's limit)
     if (p.m <= 1) return launch_gemv_any<1, true>(p, s);

@@ -104,6 +104,10 @@ cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const 
 // After a GEMM with split > 1: add each split tile's parts and finish it.
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s);
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
+// The streamed small-M form (m <= 4, Q4_K or Q6_K by p.q6); leaves *launched
+// false, launching nothing, when the call is outside its range or its shared
+// memory would not fit.
+cudaError_t launch_gemv_stream(const GemvParams& p, cudaStream_t s, bool* launched);
 // Q6_K small-M product (p.q6 set); gemv_q6k_fits says whether m tokens of k
 // activations fit its shared memory
 bool gemv_q6k_fits(int m, int64_t k);
