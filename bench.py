@@ -70,6 +70,12 @@ WORKLOADS = {
                    "7B linear stack at decode size with Q6_K weights (5.31 GB): 32 layers x {q,k,v,o 4096x4096; "
                    "gate,up 11008x4096; down 4096x11008}, 1 token, fused q8 activation quantization, bf16 out "
                    "(Q6_K small-M path, CUDA-graph replay)"),
+    "decode_fused": (1, [(n, k) for _ in range(32) for (n, k) in ((12288, 4096), (4096, 4096), (22016, 4096),
+                                                                   (4096, 11008))], "bf16",
+                     "7B linear stack at decode size with the projections that read the same input stored as one "
+                     "matrix, as decoders deploy them: 32 layers x {q|k|v 12288x4096; o 4096x4096; gate|up "
+                     "22016x4096; down 4096x11008} Q4_K (the same 3.64 GB of weights as decode, 4 launches a "
+                     "layer instead of 7), 1 token, fused q8, bf16 out (small-M path, CUDA-graph replay)"),
     "decode_gate": (1, [(11008, 4096)], "bf16",
                     "7B FFN gate projection 11008x4096 Q4_K at decode size: 1 token, fused q8, bf16 out "
                     "(small-M path, CUDA-graph replay)"),

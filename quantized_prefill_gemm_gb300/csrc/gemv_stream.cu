@@ -10,27 +10,29 @@
 // by the part of each launch that streams nothing (launch, first loads, the
 // row sums, the tail).  So:
 //
-//   - two CTAs of 256 threads per SM (grid G = min(row groups, 2 x SMs)); CTA b
-//     owns the 16-row groups b, b + G, b + 2G, ..., every group over all of
+//   - two CTAs of 256 threads per SM (grid G = min(row groups, 2 x SMs)); CTA
+//     b owns the 16-row groups b, b + G, b + 2G, ..., every group over all of
 //     k, so no partial sum leaves the CTA, and the CTAs working at the same
 //     time read neighbouring slices of the same 128-row records;
 //   - the CTA's weights flow through a ring of R stages (a few super-blocks
-//     of one group each) filled with 16-byte cp.async copies, R-1 stages in
+//     of one group each) filled with 16-byte cp.async copies whose source
+//     addresses are fixed per thread up to a per-stage offset, R-1 stages in
 //     flight while one is consumed; their completion is the hardware's
 //     wait_group, so no thread spins on a flag;
-//   - a CTA takes under a third of an SM (256 threads, about 70 KB of shared
-//     memory), so a CTA of the next launch is resident while this one runs.  Launched with programmatic dependent launch, each asks L2 for a
-//     1/G slice of its launch's weights (a prefetch hint: it cannot change
-//     what a later load returns) and only then waits for the kernel before
-//     it, so the weights come from HBM while that kernel finishes.  Every
-//     read of the ring or of the activations comes after the wait.
+//   - launched with programmatic dependent launch: as soon as a CTA is
+//     resident it asks L2 for its 1/G share of the launch's weights (a
+//     prefetch hint: it cannot change what a later load returns) and only
+//     then waits for the kernel before it, so the weights come from HBM while
+//     that kernel finishes.  Every read of the ring or of the activations
+//     comes after the wait.
 //
 // Q4_K without unpacking: in a packed quant word the nibbles of k = 0,4,1,5
 // sit at bits 0, 8, 16, 24 and those of k = 2,6,3,7 at bits 4, 12, 20, 28
-// (the word layout of the packed format), so w & 0x0F0F0F0F and
-// (w >> 4) & 0x0F0F0F0F are byte vectors dp4a takes as they are, against the
-// activations staged with each 8-byte group reordered to k = 0,4,1,5,2,6,3,7.
-// The integer dot product is the same sum in another order.
+// (the word layout of the packed format), so w & 0x0F0F0F0F is a byte vector
+// dp4a takes as it is, and w & 0xF0F0F0F0 one of 16 x the other nibbles
+// (unsigned bytes), against the activations staged with each 8-byte group
+// reordered to k = 0,4,1,5,2,6,3,7.  The integer dot product is the same sum
+// in another order.
 //
 // Thread t takes row r = t % 16 of the group and the stage's chunks
 // (t / 16) * I .. + I - 1 (I = 4 for Q4_K, 2 for Q6_K; one super-block); a
@@ -63,10 +65,10 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Ask L2 for this CTA's share of one packed array: its 4 KB pages b, b + G,
-// b + 2G, ... (over the grid, the whole array; no division on the way).
+// b + 2G, ... (over the grid, the whole array), issued by the first warp.
 __device__ __forceinline__ void prefetch_pages(const void* base, int64_t bytes, int b, int G) {
     const int64_t pages = (bytes + 4095) >> 12;
-    for (int64_t pg = b + static_cast<int64_t>(G) * threadIdx.x; pg < pages; pg += static_cast<int64_t>(G) * kThreads) {
+    for (int64_t pg = b + static_cast<int64_t>(G) * (threadIdx.x & 31); pg < pages; pg += 32 * static_cast<int64_t>(G)) {
         const int64_t off = pg << 12;
         prefetch_l2(static_cast<const uint8_t*>(base) + off, static_cast<uint32_t>(bytes - off < 4096 ? bytes - off : 4096));
     }
@@ -86,23 +88,65 @@ struct Q4Stream {
     static constexpr int kStageSb = 8;
     static constexpr int kItems = 4;
     static constexpr bool kPermuted = true;   // activations staged in the nibble order
-    static constexpr int kArrays = 5;         // nib, sc, m, d, dmin
     static constexpr uint32_t kNib = 0;
     static constexpr uint32_t kSc = kNib + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kMq = kSc + 8 * kStageSb * kRows;
     static constexpr uint32_t kD = kMq + 8 * kStageSb * kRows;
     static constexpr uint32_t kDmin = kD + kStageSb * kRows * 4;
     static constexpr uint32_t kSlot = kDmin + kStageSb * kRows * 4;
-    __host__ __device__ static constexpr int bpr(int a) { return a == 0 ? 16 : a < 3 ? 1 : 4; }
-    __host__ __device__ static constexpr bool per_sb(int a) { return a >= 3; }
-    __host__ __device__ static constexpr uint32_t smem_off(int a) {
-        return a == 0 ? kNib : a == 1 ? kSc : a == 2 ? kMq : a == 3 ? kD : kDmin;
-    }
-    __device__ static const void* base(const GemvParams& p, int a) {
-        return a == 0 ? static_cast<const void*>(p.nib) : a == 1 ? static_cast<const void*>(p.sc)
-             : a == 2 ? static_cast<const void*>(p.mq) : a == 3 ? static_cast<const void*>(p.dsb)
-                      : static_cast<const void*>(p.dmn);
-    }
+    // What thread t copies of every stage (1216 16-byte pieces): the quants
+    // of chunks t/16 + 16h (h < 4), row slice t%16, and for t < 192 one
+    // piece of the sc, m, d or dmin records.  Only the stage bases move.
+    struct Copier {
+        const uint8_t* q;   // this thread's first quant piece of the next stage
+        const uint8_t* x;   // its scale piece, or null
+        uint32_t qdst, xdst;
+        int qu, xu;         // chunk of the first quant piece; chunk (sc, m) or super-block (d, dmin) of the scale piece
+        bool xsb;           // the scale piece is per super-block
+        uint32_t xstep;
+
+        __device__ void init() {
+            const int t = threadIdx.x;
+            qu = t >> 4;
+            qdst = kNib + 16 * t;
+            x = nullptr;
+            xu = 0;
+            xsb = false;
+            xstep = 0;
+            xdst = 0;
+            if (t < 128) {
+                xu = t & 63;
+                xdst = (t < 64 ? kSc : kMq) + 16 * xu;
+                xstep = 8 * kStageSb * 128;
+            } else if (t < 192) {
+                const int q = t & 31;
+                xu = q >> 2;
+                xsb = true;
+                xdst = (t < 160 ? kD : kDmin) + 16 * q;
+                xstep = kStageSb * 128 * 4;
+            }
+        }
+        // first stage of the group of rows r0 .. r0 + 15 of tile nt
+        __device__ void group(const GemvParams& p, int64_t nt, int r0) {
+            const int t = threadIdx.x;
+            q = p.nib + ((nt * p.kc + qu) * 128 + r0 + (t & 15)) * 16;
+            if (t < 128) {
+                x = (t < 64 ? p.sc : p.mq) + (nt * p.kc + xu) * 128 + r0;
+            } else if (t < 192) {
+                const float* b = t < 160 ? p.dsb : p.dmn;
+                x = reinterpret_cast<const uint8_t*>(b + (nt * p.ksb + xu) * 128 + r0) + 16 * (t & 3);
+            }
+        }
+        // the stage of ns super-blocks into the ring slot at shared address slot; then on to the next stage
+        __device__ void issue(uint32_t slot, int ns) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                if (qu + 16 * h < 8 * ns) cp_async16(slot + qdst + 4096 * h, q + 32768 * h);
+            if (x && xu < (xsb ? ns : 8 * ns)) cp_async16(slot + xdst, x);
+            q += 8 * kStageSb * 2048;
+            if (x) x += xstep;
+        }
+    };
     __device__ static void prefetch(const GemvParams& p, int b, int G) {
         const int64_t n = p.n;
         prefetch_pages(p.nib, n * p.k / 2, b, G);
@@ -173,16 +217,59 @@ struct Q6Stream {
     static constexpr uint32_t kD = kSc + 8 * kStageSb * kRows * 2;
     static constexpr uint32_t kSlot = kD + kStageSb * kRows * 4;
 
-    static constexpr int kArrays = 4;         // lo, hi, the scale pair, d
-    __host__ __device__ static constexpr int bpr(int a) { return a == 0 ? 16 : a == 1 ? 8 : a == 2 ? 2 : 4; }
-    __host__ __device__ static constexpr bool per_sb(int a) { return a == 3; }
-    __host__ __device__ static constexpr uint32_t smem_off(int a) {
-        return a == 0 ? kLo : a == 1 ? kHi : a == 2 ? kSc : kD;
-    }
-    __device__ static const void* base(const GemvParams& p, int a) {
-        return a == 0 ? static_cast<const void*>(p.nib) : a == 1 ? static_cast<const void*>(p.q6hi)
-             : a == 2 ? static_cast<const void*>(p.sc) : static_cast<const void*>(p.dsb);
-    }
+    // What thread t copies of every stage (848 16-byte pieces): the low
+    // nibbles of chunks t/16 and t/16 + 16, row slice t%16; the high bits of
+    // chunk t/8, slice t%8; and for t < 80 one piece of the scale pairs or d.
+    struct Copier {
+        const uint8_t* lo;
+        const uint8_t* hi;
+        const uint8_t* x;   // scale-pair or d piece, or null
+        uint32_t xdst;
+        int lu, hu, xu;     // chunks of the lo and hi pieces; chunk or super-block of the x piece
+        bool xsb;
+        uint32_t xstep;
+
+        __device__ void init() {
+            const int t = threadIdx.x;
+            lu = t >> 4;
+            hu = t >> 3;
+            x = nullptr;
+            xu = 0;
+            xsb = false;
+            xstep = 0;
+            xdst = 0;
+            if (t < 64) {
+                xu = t >> 1;
+                xdst = kSc + 16 * t;
+                xstep = 8 * kStageSb * 128 * 2;
+            } else if (t < 80) {
+                const int q = t - 64;
+                xu = q >> 2;
+                xsb = true;
+                xdst = kD + 16 * q;
+                xstep = kStageSb * 128 * 4;
+            }
+        }
+        __device__ void group(const GemvParams& p, int64_t nt, int r0) {
+            const int t = threadIdx.x;
+            lo = p.nib + ((nt * p.kc + lu) * 128 + r0 + (t & 15)) * 16;
+            hi = p.q6hi + ((nt * p.kc + hu) * 128 + r0) * 8 + 16 * (t & 7);
+            if (t < 64)
+                x = p.sc + ((nt * p.kc + xu) * 128 + r0) * 2 + 16 * (t & 1);
+            else if (t < 80)
+                x = reinterpret_cast<const uint8_t*>(p.dsb + (nt * p.ksb + xu) * 128 + r0) + 16 * (t & 3);
+        }
+        __device__ void issue(uint32_t slot, int ns) {
+            const int t = threadIdx.x;
+            if (lu < 8 * ns) cp_async16(slot + kLo + 16 * t, lo);
+            if (lu + 16 < 8 * ns) cp_async16(slot + kLo + 16 * t + 4096, lo + 32768);
+            if (hu < 8 * ns) cp_async16(slot + kHi + 16 * t, hi);
+            if (x && xu < (xsb ? ns : 8 * ns)) cp_async16(slot + xdst, x);
+            lo += 8 * kStageSb * 2048;
+            hi += 8 * kStageSb * 1024;
+            if (x) x += xstep;
+        }
+    };
     __device__ static void prefetch(const GemvParams& p, int b, int G) {
         const int64_t n = p.n;
         prefetch_pages(p.nib, n * p.k / 2, b, G);
@@ -233,81 +320,14 @@ struct Q6Stream {
     }
 };
 
-// The 16-byte pieces this thread copies for every stage.  A full stage's
-// pieces are numbered array by array (each array's records in order, kBpr
-// pieces a record) and piece i is copied by thread i % 256; what a thread
-// owns is worked out once, and per stage only its source pointers move on.
-template <class F>
-__host__ __device__ constexpr int stage_pieces() {
-    int n = 0;
-    for (int a = 0; a < F::kArrays; ++a) n += (F::per_sb(a) ? 1 : 8) * F::kStageSb * F::bpr(a);
-    return n;
-}
-
-template <class F>
-struct Pieces {
-    static constexpr int kPer = (stage_pieces<F>() + kThreads - 1) / kThreads;
-    const uint8_t* src[kPer];   // the piece of the next stage issued
-    uint32_t dst[kPer];         // its offset in a ring slot
-    int arr[kPer];              // its array, -1 for none
-    int off[kPer];              // its offset from the array's first record (row r0) of a stage
-    int usb[kPer];              // its super-block within a stage (copied while usb < the stage's super-blocks)
-    int step[kPer];             // bytes from one stage's piece to the next one's
-
-    __device__ void init() {
-#pragma unroll
-        for (int h = 0; h < kPer; ++h) {
-            int i = threadIdx.x + kThreads * h;
-            arr[h] = -1;
-            dst[h] = 0;
-            off[h] = 0;
-            usb[h] = 0;
-            step[h] = 0;
-            src[h] = nullptr;
-#pragma unroll
-            for (int a = 0; a < F::kArrays; ++a) {
-                const int n = (F::per_sb(a) ? 1 : 8) * F::kStageSb * F::bpr(a);
-                if (arr[h] < 0 && i < n) {
-                    const int u = i / F::bpr(a), part = i % F::bpr(a);
-                    arr[h] = a;
-                    dst[h] = F::smem_off(a) + 16 * i;
-                    off[h] = u * 128 * F::bpr(a) + 16 * part;
-                    usb[h] = F::per_sb(a) ? u : u >> 3;
-                    step[h] = (F::per_sb(a) ? 1 : 8) * F::kStageSb * 128 * F::bpr(a);
-                }
-                if (arr[h] < 0) i -= n;
-            }
-        }
-    }
-    // first stage of the 16-row group at rows row0 (tile nt, row r0 in it)
-    __device__ void group(const GemvParams& p, int64_t nt, int r0) {
-#pragma unroll
-        for (int h = 0; h < kPer; ++h) {
-#pragma unroll
-            for (int a = 0; a < F::kArrays; ++a) {
-                if (arr[h] == a) {
-                    const int64_t rec = F::per_sb(a) ? nt * p.ksb : nt * p.kc;
-                    src[h] = static_cast<const uint8_t*>(F::base(p, a)) + (rec * 128 + r0) * F::bpr(a) + off[h];
-                }
-            }
-        }
-    }
-    // copy the stage of ns super-blocks into the slot at smem address slot, then step to the next stage
-    __device__ void issue(uint32_t slot, int ns) {
-#pragma unroll
-        for (int h = 0; h < kPer; ++h) {
-            if (arr[h] >= 0 && usb[h] < ns) cp_async16(slot + dst[h], src[h]);
-            src[h] += step[h];
-        }
-    }
-};
-
-// Ring depth: as many stages as fit in 58 KB (at least 3), so that two CTAs of
-// this launch and one of the next share an SM for k up to 11008 at m = 1
-// (measured: two CTAs of a launch per SM beat one or three).
+// Ring depth: as many stages as fit in 76 KB (at least 3).  With the staged
+// activations that is just over a third of an SM's shared memory at m = 1, so
+// two CTAs of a launch share an SM and a third cannot join them (measured:
+// better than a 58 KB ring that lets three in, and than one or three CTAs
+// per SM by grid size).
 template <class F, int M>
 __host__ __device__ constexpr int ring_depth() {
-    return 58 * 1024 / F::kSlot < 3 ? 3 : 58 * 1024 / F::kSlot;
+    return 76 * 1024 / F::kSlot < 3 ? 3 : 76 * 1024 / F::kSlot;
 }
 
 // ------------------------------------------------------------- layout --
@@ -426,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
     // the next launch may start now; L2 is asked for this CTA's slice of the
     // weights (a hint; the copies below read after the wait)
     griddep_launch_dependents();
-    F::prefetch(p, blockIdx.x, gridDim.x);
+    if (threadIdx.x < 32) F::prefetch(p, blockIdx.x, gridDim.x);
     griddep_wait();
 
     // the stage the copies are issued for: group ig, super-blocks from isb
-    Pieces<F> pc;
+    typename F::Copier pc;
     pc.init();
     int ig = g0, isb = 0, islot = 0, issued = 0;
     if (nst > 0) pc.group(p, (static_cast<int64_t>(ig) * kRows) >> 7, (ig * kRows) & 127);
