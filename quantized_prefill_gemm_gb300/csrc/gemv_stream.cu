@@ -82,12 +82,24 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     return d;
 }
 
+// Q6_K quants q = u ^ 32 (0..63, unsigned bytes) of one packed 8-k group from
+// its low-nibble word and its 2-bit high fields hf (at the group's nibble
+// positions, low two bits of each nibble), in the two permuted byte orders
+// of the Q4_K masks: q0 for k = 0,4,1,5, q1 for k = 2,6,3,7.  hf ^ 0x22..
+// flips bit 5 of u in both.
+__device__ __forceinline__ void q6_bytes(uint32_t lo, uint32_t hf, uint32_t& q0, uint32_t& q1) {
+    const uint32_t hx = hf ^ 0x22222222u;
+    q0 = (lo & kLowNibbles) | ((hx << 4) & 0x30303030u);
+    q1 = ((lo >> 4) & kLowNibbles) | (hx & 0x30303030u);
+}
+
 // Q4_K: nib 16 B, sc 1 B, m 1 B per (row, chunk); d, dmin fp32 per (row, sb).
 // A stage is 8 super-blocks; a thread takes 4 chunks of one super-block.
 struct Q4Stream {
     static constexpr int kStageSb = 8;
     static constexpr int kItems = 4;
     static constexpr bool kPermuted = true;   // activations staged in the nibble order
+    static constexpr bool kHalfSums = false;  // staged: d_a * ssum
     static constexpr uint32_t kNib = 0;
     static constexpr uint32_t kSc = kNib + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kMq = kSc + 8 * kStageSb * kRows;
@@ -210,7 +222,8 @@ struct Q4Stream {
 struct Q6Stream {
     static constexpr int kStageSb = 4;
     static constexpr int kItems = 2;
-    static constexpr bool kPermuted = false;
+    static constexpr bool kPermuted = true;
+    static constexpr bool kHalfSums = true;   // staged: the two half-chunk code sums
     static constexpr uint32_t kLo = 0;
     static constexpr uint32_t kHi = kLo + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kSc = kHi + 8 * kStageSb * kRows * 8;
@@ -277,7 +290,8 @@ struct Q6Stream {
         prefetch_pages(p.sc, n * p.kc * 2, b, G);
         prefetch_pages(p.dsb, n * p.ksb * 4, b, G);
     }
-    // I = sc_0 * sum_{k<16} (q-32) qa + sc_1 * sum_{k>=16} (q-32) qa (|I| < 2^24, exact in fp32)
+    // I = sc_0 * sum_{k<16} (q-32) qa + sc_1 * sum_{k>=16} (q-32) qa (|I| < 2^24, exact in fp32), as
+    // sc_h * (sum q qa - 32 X_h) with q the unsigned 6-bit quants and X_h the half's code sum
     template <int M>
     __device__ static void compute(const uint8_t* sl, int j0, int r, int c0, const int8_t* act, const float2* xs,
                                    int m, int k, int kc, float (&acc)[M]) {
@@ -290,11 +304,11 @@ struct Q6Stream {
             const uint4 lo = *reinterpret_cast<const uint4*>(sl + kLo + (j * kRows + r) * 16);
             const uint2 hi = *reinterpret_cast<const uint2*>(sl + kHi + (j * kRows + r) * 8);
             const uint32_t scp = *reinterpret_cast<const uint16_t*>(sl + kSc + (j * kRows + r) * 2);
-            uint32_t v[8];
-            unpack_q6(lo.x, hi.x, v[0], v[1]);
-            unpack_q6(lo.y, hi.x >> 2, v[2], v[3]);
-            unpack_q6(lo.z, hi.y, v[4], v[5]);
-            unpack_q6(lo.w, hi.y >> 2, v[6], v[7]);
+            uint32_t q[8];
+            q6_bytes(lo.x, hi.x, q[0], q[1]);
+            q6_bytes(lo.y, hi.x >> 2, q[2], q[3]);
+            q6_bytes(lo.z, hi.y, q[4], q[5]);
+            q6_bytes(lo.w, hi.y >> 2, q[6], q[7]);
             const int sc0 = static_cast<int>(static_cast<int8_t>(scp & 0xFFu));
             const int sc1 = static_cast<int>(static_cast<int8_t>(scp >> 8));
 #pragma unroll
@@ -302,15 +316,19 @@ struct Q6Stream {
                 if (t < m) {
                     const int4* a = reinterpret_cast<const int4*>(act + static_cast<int64_t>(t) * k + 32 * c);
                     const int4 a0 = a[0], a1 = a[1];
-                    int J0 = __dp4a(static_cast<int>(v[0]), a0.x, 0);
-                    J0 = __dp4a(static_cast<int>(v[1]), a0.y, J0);
-                    J0 = __dp4a(static_cast<int>(v[2]), a0.z, J0);
-                    J0 = __dp4a(static_cast<int>(v[3]), a0.w, J0);
-                    int J1 = __dp4a(static_cast<int>(v[4]), a1.x, 0);
-                    J1 = __dp4a(static_cast<int>(v[5]), a1.y, J1);
-                    J1 = __dp4a(static_cast<int>(v[6]), a1.z, J1);
-                    J1 = __dp4a(static_cast<int>(v[7]), a1.w, J1);
-                    P[t] = fmaf(xs[t * kc + c].x, static_cast<float>(sc0 * J0 + sc1 * J1), P[t]);
+                    int J0 = dp4a_us(q[0], a0.x, 0);
+                    int J1 = dp4a_us(q[4], a1.x, 0);
+                    J0 = dp4a_us(q[1], a0.y, J0);
+                    J1 = dp4a_us(q[5], a1.y, J1);
+                    J0 = dp4a_us(q[2], a0.z, J0);
+                    J1 = dp4a_us(q[6], a1.z, J1);
+                    J0 = dp4a_us(q[3], a0.w, J0);
+                    J1 = dp4a_us(q[7], a1.w, J1);
+                    const float2 s = xs[t * kc + c];
+                    const int xp = __float_as_int(s.y);
+                    const int X0 = (xp << 16) >> 16, X1 = xp >> 16;
+                    const int I = sc0 * (J0 - 32 * X0) + sc1 * (J1 - 32 * X1);
+                    P[t] = fmaf(s.x, static_cast<float>(I), P[t]);
                 }
             }
         }
@@ -354,8 +372,9 @@ __device__ __forceinline__ void permute_group(uint32_t lo, uint32_t hi, uint32_t
 
 // Stage the m x k activations: the q8 SoA copied, or fp32 rows quantized by
 // the q8 rule (a 32-element block per pair of threads); with each block's d_a
-// and d_a * ssum as fp32.
-template <bool kQuant, bool kPermuted>
+// and either d_a * ssum as fp32 (Q4_K) or the code sums of its two 16-element
+// halves as two int16 in the bits of the second float (Q6_K).
+template <bool kQuant, bool kPermuted, bool kHalfSums>
 __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, float2* xs) {
     const int kc = p.kc, m = p.m, k = p.k;
     if constexpr (kQuant) {
@@ -383,22 +402,25 @@ __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, flo
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
             const Q8Scale s = q8_scale(amax);
             uint32_t w[4] = {0u, 0u, 0u, 0u};
-            int sum = 0;
+            int own = 0;   // this half's sum of codes
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int q = q8_code(v[e], s);
-                sum += q;
+                own += q;
                 w[e >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e & 3));
             }
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+            const int sum = own + __shfl_xor_sync(0xFFFFFFFFu, own, 1);
             if constexpr (kPermuted) {
                 permute_group(w[0], w[1], w[0], w[1]);
                 permute_group(w[2], w[3], w[2], w[3]);
             }
             if (live) {
                 reinterpret_cast<uint4*>(act + static_cast<int64_t>(t) * k + 32 * c)[half] = make_uint4(w[0], w[1], w[2], w[3]);
-                if (half == 0) {
-                    const float da = __half2float(s.da);
+                const float da = __half2float(s.da);
+                if constexpr (kHalfSums) {
+                    reinterpret_cast<int16_t*>(&xs[t * kc + c].y)[half] = static_cast<int16_t>(own);
+                    if (half == 0) xs[t * kc + c].x = da;
+                } else if (half == 0) {
                     xs[t * kc + c] = make_float2(da, da * static_cast<float>(sum));
                 }
             }
@@ -408,6 +430,11 @@ __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, flo
         for (int i = threadIdx.x; i < m * v16; i += kThreads) {
             const int t = i / v16, j = i - t * v16;
             uint4 w = __ldg(reinterpret_cast<const uint4*>(p.q8 + t * p.ldq) + j);
+            if constexpr (kHalfSums) {   // piece j is half j % 2 of chunk j / 2
+                const int hs = __dp4a(static_cast<int>(w.x), 0x01010101, __dp4a(static_cast<int>(w.y), 0x01010101,
+                               __dp4a(static_cast<int>(w.z), 0x01010101, __dp4a(static_cast<int>(w.w), 0x01010101, 0))));
+                reinterpret_cast<int16_t*>(&xs[t * kc + (j >> 1)].y)[j & 1] = static_cast<int16_t>(hs);
+            }
             if constexpr (kPermuted) {
                 permute_group(w.x, w.y, w.x, w.y);
                 permute_group(w.z, w.w, w.z, w.w);
@@ -417,8 +444,12 @@ __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, flo
         for (int i = threadIdx.x; i < m * kc; i += kThreads) {
             const int t = i / kc, c = i - t * kc;
             const float da = __half2float(__ushort_as_half(__ldg(p.da + t * kc + c)));
-            const float ss = p.ssum ? static_cast<float>(__ldg(p.ssum + t * kc + c)) : 0.0f;
-            xs[t * kc + c] = make_float2(da, da * ss);
+            if constexpr (kHalfSums) {
+                xs[t * kc + c].x = da;
+            } else {
+                const float ss = static_cast<float>(__ldg(p.ssum + t * kc + c));
+                xs[t * kc + c] = make_float2(da, da * ss);
+            }
         }
     }
 }
@@ -470,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
     };
 #pragma unroll 1
     for (int s = 0; s < R - 1; ++s) issue();
-    stage_acts<kQuant, F::kPermuted>(p, act, reinterpret_cast<float2*>(smem_raw + L.xs));
+    stage_acts<kQuant, F::kPermuted, F::kHalfSums>(p, act, reinterpret_cast<float2*>(smem_raw + L.xs));
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = threadIdx.x & 15;
