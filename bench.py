@@ -187,8 +187,8 @@ TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "traffic__q4k_gemm_kernel.txt")
 def gemm_traffic(mats, tokens, q6):
     """DRAM bytes per GEMM launch, averaged over the step's launches, from the
     per-shape ncu captures in profiles/ (lines "M N K bytes"), valid only for
-    the kernel build they were taken on ("digest" line = the build's source
-    digest).  Returns (bytes or None, note)."""
+    the GEMM kernel build they were taken on ("digest" line = the hash of the
+    GEMM's sources and flags, build.gemm_digest()).  Returns (bytes or None, note)."""
     from quantized_prefill_gemm_gb300 import build as qbuild
 
     if q6:
@@ -205,7 +205,7 @@ def gemm_traffic(mats, tokens, q6):
                 digest = parts[1]
             elif len(parts) == 4 and all(p.isdigit() for p in parts):
                 shapes[tuple(int(p) for p in parts[:3])] = int(parts[3])
-    if digest != qbuild._digest():
+    if digest != qbuild.gemm_digest():
         return None, "kernel changed since the ncu capture (digest mismatch)"
     try:
         vals = [shapes[(tokens, n, k)] for n, k in mats]

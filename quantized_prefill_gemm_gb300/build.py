@@ -48,6 +48,20 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def gemm_digest() -> str:
+    """Hash of what the tensor-core GEMM kernel is built from: gemm.cu, the
+    headers it includes, and the flags.  Measurements of that kernel (the
+    per-shape DRAM traffic table under profiles/) are keyed by it, so they
+    stay valid while other kernels change."""
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "q4k_internal.h", "q4k_layout.h", "q4k_ptx.cuh", "q4k_unpack.cuh", "q8_rule.cuh"):
+        h.update(f.encode())
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + [c for c in CFLAGS if not c.startswith("-I")]).encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     """Compile and link; return the library path."""
     extra = list(extra_flags or [])

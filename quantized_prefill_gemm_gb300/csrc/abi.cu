@@ -11,6 +11,7 @@
 
 #include "../../include/q4k.h"
 #include "q4k_internal.h"
+#include "q4k_gemv.h"
 #include "q4k_layout.h"
 
 namespace q4k {

@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 
 #include "q4k_internal.h"
+#include "q4k_gemv.h"
 #include "q4k_ptx.cuh"
 #include "q8_rule.cuh"
 #include "q4k_unpack.cuh"

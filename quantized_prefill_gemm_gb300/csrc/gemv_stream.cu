@@ -43,6 +43,7 @@
 #include <algorithm>
 
 #include "q4k_internal.h"
+#include "q4k_gemv.h"
 #include "q4k_ptx.cuh"
 #include "q8_rule.cuh"
 #include "q4k_unpack.cuh"
