@@ -39,6 +39,7 @@
 // of a per-chunk scheme; those hand-offs, not the tensor pipe, bound the loop.
 // Every wait is bounded (q4k_ptx.cuh: mbar_wait): a stuck pipeline records an
 // error word and the CTA leaves through the normal teardown.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -950,17 +951,17 @@ __global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_cycles) {
 template <bool kDump, bool kSwiGLU, bool kQ6>
 cudaError_t launch_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                            const GemmParams& p, int grid, cudaStream_t s) {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];   // zero at start; a race only repeats the call
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     constexpr size_t smem = Lay<kQ6>::kSmemBytes;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(q4k_gemm_kernel<kDump, kSwiGLU, kQ6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     return launch_pdl(q4k_gemm_kernel<kDump, kSwiGLU, kQ6>, dim3(grid), dim3(kThreads), smem, s, tm_x, tm_e, tm_d, p);
 }

@@ -31,6 +31,7 @@
 // dp4a), P[t] += d_a[t] * (sc * J[t]) (sc*J < 2^22 is exact in fp32),
 // Z[t] += (d_a[t] * ssum[t]) * (-dmin * m) (both factors exact in fp32); per
 // super-block Y[t] += d * P[t].
+#include <atomic>
 #include <cuda_bf16.h>
 #include <algorithm>
 #include <cuda_fp16.h>
@@ -566,18 +567,18 @@ __global__ void __launch_bounds__(kThreads, M == 1 ? 2 : 1) q6k_gemv_persistent_
 
 template <int M, bool kQuant>
 cudaError_t launch_q6k_gemv_m(const GemvParams& p, cudaStream_t s) {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];   // zero at start; a race only repeats the call
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const size_t smem = PersistSmem(M, p.k).total;
     if (smem > kPersistMaxSmem) return cudaErrorInvalidValue;   // the caller checks the size first
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(q6k_gemv_persistent_kernel<M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kPersistMaxSmem));
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -594,18 +595,18 @@ cudaError_t launch_q6k_gemv_m(const GemvParams& p, cudaStream_t s) {
 template <int M, bool kQuant>
 cudaError_t launch_gemv_persistent(const GemvParams& p, cudaStream_t s, bool* launched) {
     *launched = false;
-    static size_t smem_set[64] = {};
+    static std::atomic<size_t> smem_set[64];   // zero at start; a race only repeats the call
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const size_t smem = PersistSmem(M, p.k).total;
     if (smem > kPersistMaxSmem) return cudaSuccess;   // too large: the caller uses the other form
-    if (smem_set[dev] < smem) {   // raise the kernel's dynamic shared memory limit once per size class
+    if (smem_set[dev].load(std::memory_order_acquire) < smem) {   // raise the limit once per size class
         e = cudaFuncSetAttribute(q4k_gemv_persistent_kernel<M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kPersistMaxSmem));
         if (e != cudaSuccess) return e;
-        smem_set[dev] = kPersistMaxSmem;
+        smem_set[dev].store(kPersistMaxSmem, std::memory_order_release);
     }
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -626,16 +627,16 @@ cudaError_t launch_gemv_persistent(const GemvParams& p, cudaStream_t s, bool* la
 
 template <int M, bool kQuant>
 cudaError_t launch_gemv_m(const GemvParams& p, cudaStream_t s) {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];   // zero at start; a race only repeats the call
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     constexpr size_t smem = gemv_smem_bytes<M>();
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(q4k_gemv_kernel<M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.n / kRows));

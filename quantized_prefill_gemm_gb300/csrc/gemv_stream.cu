@@ -38,6 +38,7 @@
 // (t / 16) * I .. + I - 1 (I = 4 for Q4_K, 2 for Q6_K; one super-block); a
 // row's sums are added over its 16 threads (a shuffle, then 8 warps' partials
 // in shared memory in a fixed order) at the end of each group and stored.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <algorithm>
@@ -95,10 +96,12 @@ __device__ __forceinline__ void q6_bytes(uint32_t lo, uint32_t hf, uint32_t& q0,
 }
 
 // Q4_K: nib 16 B, sc 1 B, m 1 B per (row, chunk); d, dmin fp32 per (row, sb).
-// A stage is 8 super-blocks; a thread takes 4 chunks of one super-block.
-struct Q4Stream {
-    static constexpr int kStageSb = 8;
-    static constexpr int kItems = 4;
+// A stage is kSb super-blocks (8 in use); a thread takes kSb / 2 chunks of
+// one super-block.
+template <int kSb>
+struct Q4StreamT {
+    static constexpr int kStageSb = kSb;
+    static constexpr int kItems = kSb / 2;   // 8 kSb chunks over 16 chunk columns
     static constexpr bool kPermuted = true;   // activations staged in the nibble order
     static constexpr bool kHalfSums = false;  // staged: d_a * ssum
     static constexpr uint32_t kNib = 0;
@@ -107,9 +110,12 @@ struct Q4Stream {
     static constexpr uint32_t kD = kMq + 8 * kStageSb * kRows;
     static constexpr uint32_t kDmin = kD + kStageSb * kRows * 4;
     static constexpr uint32_t kSlot = kDmin + kStageSb * kRows * 4;
-    // What thread t copies of every stage (1216 16-byte pieces): the quants
-    // of chunks t/16 + 16h (h < 4), row slice t%16, and for t < 192 one
-    // piece of the sc, m, d or dmin records.  Only the stage bases move.
+    // What thread t copies of every stage (152 kSb 16-byte pieces): the
+    // quants of chunks t/16 + 16h (h < kSb/2), row slice t%16, and for
+    // t < 24 kSb one piece of the sc, m, d or dmin records.  Only the stage
+    // bases move.
+    static constexpr int kScPieces = 8 * kSb;   // sc (and m) pieces of a stage: one per chunk
+    static constexpr int kDPieces = 4 * kSb;    // d (and dmin) pieces: four per super-block
     struct Copier {
         const uint8_t* q;   // this thread's first quant piece of the next stage
         const uint8_t* x;   // its scale piece, or null
@@ -127,15 +133,15 @@ struct Q4Stream {
             xsb = false;
             xstep = 0;
             xdst = 0;
-            if (t < 128) {
-                xu = t & 63;
-                xdst = (t < 64 ? kSc : kMq) + 16 * xu;
+            if (t < 2 * kScPieces) {
+                xu = t % kScPieces;
+                xdst = (t < kScPieces ? kSc : kMq) + 16 * xu;
                 xstep = 8 * kStageSb * 128;
-            } else if (t < 192) {
-                const int q = t & 31;
+            } else if (t < 2 * kScPieces + 2 * kDPieces) {
+                const int q = (t - 2 * kScPieces) % kDPieces;
                 xu = q >> 2;
                 xsb = true;
-                xdst = (t < 160 ? kD : kDmin) + 16 * q;
+                xdst = (t < 2 * kScPieces + kDPieces ? kD : kDmin) + 16 * q;
                 xstep = kStageSb * 128 * 4;
             }
         }
@@ -143,17 +149,17 @@ struct Q4Stream {
         __device__ void group(const GemvParams& p, int64_t nt, int r0) {
             const int t = threadIdx.x;
             q = p.nib + ((nt * p.kc + qu) * 128 + r0 + (t & 15)) * 16;
-            if (t < 128) {
-                x = (t < 64 ? p.sc : p.mq) + (nt * p.kc + xu) * 128 + r0;
-            } else if (t < 192) {
-                const float* b = t < 160 ? p.dsb : p.dmn;
+            if (t < 2 * kScPieces) {
+                x = (t < kScPieces ? p.sc : p.mq) + (nt * p.kc + xu) * 128 + r0;
+            } else if (t < 2 * kScPieces + 2 * kDPieces) {
+                const float* b = t < 2 * kScPieces + kDPieces ? p.dsb : p.dmn;
                 x = reinterpret_cast<const uint8_t*>(b + (nt * p.ksb + xu) * 128 + r0) + 16 * (t & 3);
             }
         }
         // the stage of ns super-blocks into the ring slot at shared address slot; then on to the next stage
         __device__ void issue(uint32_t slot, int ns) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h)
+            for (int h = 0; h < kSb / 2; ++h)
                 if (qu + 16 * h < 8 * ns) cp_async16(slot + qdst + 4096 * h, q + 32768 * h);
             if (x && xu < (xsb ? ns : 8 * ns)) cp_async16(slot + xdst, x);
             q += 8 * kStageSb * 2048;
@@ -168,7 +174,7 @@ struct Q4Stream {
         prefetch_pages(p.dsb, n * p.ksb * 4, b, G);
         prefetch_pages(p.dmn, n * p.ksb * 4, b, G);
     }
-    // Row r, chunks j0 .. j0 + 3 of the stage (global chunks c0 .. c0 + 3):
+    // Row r, chunks j0 .. j0 + kItems - 1 of the stage (global chunks c0 ..):
     //   acc += d * sum_c d_a * (sc * J) - dmin * sum_c m * (d_a * ssum)
     // J = J_lo + J_hi / 16: the low nibbles as they sit, the high nibbles
     // masked in place (16 x their value, unsigned bytes); both sums exact.
@@ -217,6 +223,8 @@ struct Q4Stream {
         for (int t = 0; t < M; ++t) acc[t] = fmaf(-dmin, Z[t], fmaf(d, P[t], acc[t]));
     }
 };
+
+using Q4Stream = Q4StreamT<8>;
 
 // Q6_K: lo 16 B, hi 8 B, the two i8 scales 2 B per (row, chunk); d fp32 per
 // (row, sb).  A stage is 4 super-blocks; a thread takes 2 chunks of one.
@@ -555,16 +563,16 @@ cudaError_t launch_stream_m(const GemvParams& p, cudaStream_t s, bool* launched)
     *launched = false;
     const size_t smem = StreamSmem(M, p.k, ring_depth<F, M>(), F::kSlot).total;
     if (smem > kStreamMaxSmem) return cudaSuccess;   // too large: the caller uses another form
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];   // zero at start; a race only repeats the call
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(gemv_stream_kernel<F, M, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kStreamMaxSmem));
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;

@@ -1,12 +1,13 @@
 """q4k_gemm for decode-sized batches (1 <= m <= 16 tokens): the CUDA-core
-small-M path, compared with the oracle.
+small-M paths (the streamed kernel for m <= 4, the register-held kernels for
+5 <= m <= 16), compared with the oracle.
 
 Same bar as the GEMM: per element |y_gpu - y_oracle| <= 1e-4 * sum_k |w_k a_k|
 (plus one bf16 rounding for bf16 output).  The shapes span one and several
-128-row tiles, a super-block count that is not a multiple of the kernel's 16
-shares (k = 11008 has 43), every token count class (1, 2, 3-4, 5-8, 9-16),
-both activation forms, and q8 arrays the path cannot take directly (it then
-uses the general path).
+128-row tiles, super-block counts that fill no whole number of the kernels'
+stages or shares (k = 11008 has 43), several row groups per CTA, every token
+count class (1, 2, 3-4, 5-8, 9-16), both activation forms, and q8 arrays the
+path cannot take directly (it then uses the general path).
 """
 import numpy as np
 import pytest
@@ -71,6 +72,32 @@ def test_decode_sizes(q4k, n, k, m, out):
     last shape's 16 x 14336 activations do not fit the persistent form's
     shared memory: it takes the per-group form)."""
     _check(q4k, n, k, m, "silu_mul" if k >= 11008 else "normal", 60 + m, out=out)
+
+
+@pytest.mark.parametrize("n,k,m,out", [(4096, 11008, 1, "bf16"), (12288, 4096, 1, "bf16"),
+                                       (22016, 4096, 1, "bf16"), (128, 256, 2, "f32"), (640, 2304, 3, "f32")])
+def test_streamed_shapes(q4k, n, k, m, out):
+    """Shapes that exercise the streamed kernel (m <= 4) in particular, every
+    output checked: the 7B down projection (43 super-blocks, so each group
+    ends with a stage of 3), q|k|v and gate|up stored as one matrix (768 and
+    1376 16-row groups: several per CTA), a single super-block (a one-super-
+    block stage), and 40 groups with 9 super-blocks (a short second stage)."""
+    _check(q4k, n, k, m, "silu_mul" if k >= 11008 else "normal", 90 + m, out=out)
+
+
+def test_streamed_repeats_bitwise(q4k):
+    """Two calls of the streamed kernel give identical bits (each row is summed
+    in one CTA in a fixed order), for fp32 and for q8 input."""
+    n, k, m = 4096, 4096, 1
+    blocks, x = make_case(n, k, m, "normal", 95)
+    packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+    xd = to_dev(x)
+    q, da, ss = q4k.q8_quantize_rows(xd)
+    a = q4k.q4k_gemm(packed, n, k, xd, out_dtype="bf16")
+    b = q4k.q4k_gemm(packed, n, k, xd, out_dtype="bf16")
+    c = q4k.q4k_gemm(packed, n, k, q, out_dtype="bf16", da=da, ssum=ss)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
 
 
 def test_matches_general_path_and_repeats(q4k):
