@@ -76,6 +76,10 @@ WORKLOADS = {
                      "matrix, as decoders deploy them: 32 layers x {q|k|v 12288x4096; o 4096x4096; gate|up "
                      "22016x4096; down 4096x11008} Q4_K (the same 3.64 GB of weights as decode, 4 launches a "
                      "layer instead of 7), 1 token, fused q8, bf16 out (small-M path, CUDA-graph replay)"),
+    "decode_b8": (8, [(n, k) for _ in range(32) for (_, n, k) in LAYER], "bf16",
+                  "7B linear stack at a decode batch of 8 tokens: 32 layers x {q,k,v,o 4096x4096; gate,up "
+                  "11008x4096; down 4096x11008} Q4_K, q8 quantization pass then the small-M product, bf16 out "
+                  "(small-M path, CUDA-graph replay)"),
     "decode_gate": (1, [(11008, 4096)], "bf16",
                     "7B FFN gate projection 11008x4096 Q4_K at decode size: 1 token, fused q8, bf16 out "
                     "(small-M path, CUDA-graph replay)"),

@@ -1,5 +1,6 @@
 // Small-M (decode-sized) product with the packed weights streamed through a
-// shared-memory ring: m <= 4 tokens, Q4_K or Q6_K weights.
+// shared-memory ring: m <= 4 tokens with Q4_K or Q6_K weights (dp4a), and
+// 5..16 tokens of q8 input with Q4_K weights (integer mma.sync).
 //
 // The arithmetic is the small-M kernels' (per 32-k chunk an exact integer dot
 // product of the 4- or 6-bit quants with the q8 codes, then the block
@@ -84,6 +85,19 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     return d;
 }
 
+// One warp-level integer MMA, D = A (16 x 32 unsigned bytes) * B (32 x 8
+// signed bytes) + 0, with the fragment layout of mma.m16n8k32: lane l holds
+// A rows l/4 and l/4 + 8 at k-slots 4(l%4)..+3 (a0, a1) and 16 + 4(l%4)..+3
+// (a2, a3), B column l/4 at the same two slot groups (b0, b1), and D rows l/4
+// (d0, d1) and l/4 + 8 (d2, d3) at columns 2(l%4), 2(l%4) + 1.
+__device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%10,%11,%12,%13};"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0), "r"(0), "r"(0), "r"(0));
+}
+
 // Q6_K quants q = u ^ 32 (0..63, unsigned bytes) of one packed 8-k group from
 // its low-nibble word and its 2-bit high fields hf (at the group's nibble
 // positions, low two bits of each nibble), in the two permuted byte orders
@@ -104,6 +118,7 @@ struct Q4StreamT {
     static constexpr int kItems = kSb / 2;   // 8 kSb chunks over 16 chunk columns
     static constexpr bool kPermuted = true;   // activations staged in the nibble order
     static constexpr bool kHalfSums = false;  // staged: d_a * ssum
+    static constexpr bool kMma = true;        // 8 and 16 tokens on the tensor cores (compute_mma)
     static constexpr uint32_t kNib = 0;
     static constexpr uint32_t kSc = kNib + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kMq = kSc + 8 * kStageSb * kRows;
@@ -222,6 +237,62 @@ struct Q4StreamT {
 #pragma unroll
         for (int t = 0; t < M; ++t) acc[t] = fmaf(-dmin, Z[t], fmaf(d, P[t], acc[t]));
     }
+    // 8 or 16 tokens on the tensor cores (mma.sync m16n8k32, u8 x s8): warp w
+    // takes super-block w of the stage for all 16 rows of the group.  The A
+    // operand is 16 x the quants: for word i of a row, k-slots 4i..4i+3 hold
+    // its low nibbles shifted up and 16 + 4i..+3 its high nibbles masked in
+    // place; the B operand is the activations staged in the same permuted
+    // order (an 8-byte load gives both slot groups).  So D = 16 J exactly.
+    // acc[4 mi + e]: rows l/4 (e < 2) and l/4 + 8, tokens 8 mi + 2(l%4) + e%2.
+    template <int M>
+    __device__ static void compute_mma(const uint8_t* sl, int w, int lane, int c0, const int8_t* act, const float2* xs,
+                                       int k, int kc, float (&acc)[M / 2]) {
+        constexpr int kN = M / 8;   // n8 blocks of tokens
+        const int g = lane >> 2, q = lane & 3;
+        float P[4 * kN], Z[4 * kN];
+#pragma unroll
+        for (int i = 0; i < 4 * kN; ++i) {
+            P[i] = 0.0f;
+            Z[i] = 0.0f;
+        }
+#pragma unroll 2
+        for (int jj = 0; jj < 8; ++jj) {
+            const int j = 8 * w + jj, c = c0 + jj;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sl + kNib + (j * kRows + g) * 16 + 4 * q);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sl + kNib + (j * kRows + g + 8) * 16 + 4 * q);
+            const uint32_t a0 = (w0 << 4) & ~kLowNibbles, a1 = (w1 << 4) & ~kLowNibbles;
+            const uint32_t a2 = w0 & ~kLowNibbles, a3 = w1 & ~kLowNibbles;
+            const int sc0 = sl[kSc + j * kRows + g], sc1 = sl[kSc + j * kRows + g + 8];
+            const float m0 = static_cast<float>(sl[kMq + j * kRows + g]);
+            const float m1 = static_cast<float>(sl[kMq + j * kRows + g + 8]);
+#pragma unroll
+            for (int mi = 0; mi < kN; ++mi) {
+                const uint2 b = *reinterpret_cast<const uint2*>(act + static_cast<int64_t>(8 * mi + g) * k + 32 * c + 8 * q);
+                int d[4];
+                mma_u8s8(d, a0, a1, a2, a3, b.x, b.y);
+                const float2 s0 = xs[(8 * mi + 2 * q) * kc + c], s1 = xs[(8 * mi + 2 * q + 1) * kc + c];
+                // d / 16 = J exactly; sc * J < 2^22
+                P[4 * mi + 0] = fmaf(s0.x, static_cast<float>(sc0 * (d[0] >> 4)), P[4 * mi + 0]);
+                P[4 * mi + 1] = fmaf(s1.x, static_cast<float>(sc0 * (d[1] >> 4)), P[4 * mi + 1]);
+                P[4 * mi + 2] = fmaf(s0.x, static_cast<float>(sc1 * (d[2] >> 4)), P[4 * mi + 2]);
+                P[4 * mi + 3] = fmaf(s1.x, static_cast<float>(sc1 * (d[3] >> 4)), P[4 * mi + 3]);
+                Z[4 * mi + 0] = fmaf(s0.y, m0, Z[4 * mi + 0]);
+                Z[4 * mi + 1] = fmaf(s1.y, m0, Z[4 * mi + 1]);
+                Z[4 * mi + 2] = fmaf(s0.y, m1, Z[4 * mi + 2]);
+                Z[4 * mi + 3] = fmaf(s1.y, m1, Z[4 * mi + 3]);
+            }
+        }
+        const float* dv = reinterpret_cast<const float*>(sl + kD) + w * kRows;
+        const float* nv = reinterpret_cast<const float*>(sl + kDmin) + w * kRows;
+        const float d0 = dv[g], d1 = dv[g + 8], n0 = nv[g], n1 = nv[g + 8];
+#pragma unroll
+        for (int mi = 0; mi < kN; ++mi) {
+            acc[4 * mi + 0] = fmaf(-n0, Z[4 * mi + 0], fmaf(d0, P[4 * mi + 0], acc[4 * mi + 0]));
+            acc[4 * mi + 1] = fmaf(-n0, Z[4 * mi + 1], fmaf(d0, P[4 * mi + 1], acc[4 * mi + 1]));
+            acc[4 * mi + 2] = fmaf(-n1, Z[4 * mi + 2], fmaf(d1, P[4 * mi + 2], acc[4 * mi + 2]));
+            acc[4 * mi + 3] = fmaf(-n1, Z[4 * mi + 3], fmaf(d1, P[4 * mi + 3], acc[4 * mi + 3]));
+        }
+    }
 };
 
 using Q4Stream = Q4StreamT<8>;
@@ -233,6 +304,7 @@ struct Q6Stream {
     static constexpr int kItems = 2;
     static constexpr bool kPermuted = true;
     static constexpr bool kHalfSums = true;   // staged: the two half-chunk code sums
+    static constexpr bool kMma = false;
     static constexpr uint32_t kLo = 0;
     static constexpr uint32_t kHi = kLo + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kSc = kHi + 8 * kStageSb * kRows * 8;
@@ -351,10 +423,12 @@ struct Q6Stream {
 // activations that is just over a third of an SM's shared memory at m = 1, so
 // two CTAs of a launch share an SM and a third cannot join them (measured:
 // better than a 58 KB ring that lets three in, and than one or three CTAs
-// per SM by grid size).
+// per SM by grid size).  The 8- and 16-token forms stage 8-16 x more
+// activations; there a 58 KB ring lets two CTAs share an SM for k = 4096
+// (measured 10% faster at 8 tokens).
 template <class F, int M>
 __host__ __device__ constexpr int ring_depth() {
-    return 76 * 1024 / F::kSlot < 3 ? 3 : 76 * 1024 / F::kSlot;
+    return (M >= 8 ? 58 : 76) * 1024 / F::kSlot < 3 ? 3 : (M >= 8 ? 58 : 76) * 1024 / F::kSlot;
 }
 
 // ------------------------------------------------------------- layout --
@@ -515,9 +589,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = threadIdx.x & 15;
     const int j0 = (threadIdx.x >> 4) * F::kItems;   // this thread's first chunk in a stage
-    float acc[M];
+    constexpr bool kMma = M >= 8;                     // tensor-core form: warp w takes super-block w of a stage
+    constexpr int kAcc = kMma ? M / 2 : M;
+    float acc[kAcc];
 #pragma unroll
-    for (int t = 0; t < M; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < kAcc; ++t) acc[t] = 0.0f;
     int g = g0, sb0 = 0, slot = 0;   // the stage consumed
 #pragma unroll 1
     for (int s = 0; s < nst; ++s) {
@@ -525,17 +601,30 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
         __syncthreads();          // everyone's have; everyone is done with stage s - 1 (and the activations are staged)
         issue();                  // into the slot stage s - 1 used
         const int nch = 8 * min(kSb, ksb - sb0);
-        if (j0 < nch)
-            F::template compute<M>(smem_raw + L.ring + static_cast<size_t>(slot) * F::kSlot, j0, r, 8 * sb0 + j0, act,
-                                   xs, m, k, kc, acc);
+        const uint8_t* sl = smem_raw + L.ring + static_cast<size_t>(slot) * F::kSlot;
+        if constexpr (kMma) {
+            if (8 * warp < nch) F::template compute_mma<M>(sl, warp, lane, 8 * (sb0 + warp), act, xs, k, kc, acc);
+        } else {
+            if (j0 < nch) F::template compute<M>(sl, j0, r, 8 * sb0 + j0, act, xs, m, k, kc, acc);
+        }
         slot = slot + 1 == R ? 0 : slot + 1;
         sb0 += kSb;
-        if (sb0 >= ksb) {   // the group's last stage: add the 32 threads of each row, store
+        if (sb0 >= ksb) {   // the group's last stage: add the partial sums of each (token, row), store
+            if constexpr (kMma) {   // each warp's (its super-blocks') sums, [warp][token][row]
+                const int g = lane >> 2, q = lane & 3;
 #pragma unroll
-            for (int t = 0; t < M; ++t) {
-                acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], 16);
-                if (lane < 16) red[(warp * M + t) * kRows + r] = acc[t];
-                acc[t] = 0.0f;
+                for (int i = 0; i < kAcc; ++i) {
+                    const int tok = 8 * (i >> 2) + 2 * q + (i & 1), row = g + 8 * ((i >> 1) & 1);
+                    red[(warp * M + tok) * kRows + row] = acc[i];
+                    acc[i] = 0.0f;
+                }
+            } else {   // the two half-warps of a row, then each warp's sums
+#pragma unroll
+                for (int t = 0; t < M; ++t) {
+                    acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], 16);
+                    if (lane < 16) red[(warp * M + t) * kRows + r] = acc[t];
+                    acc[t] = 0.0f;
+                }
             }
             __syncthreads();
             if (threadIdx.x < M * kRows) {
@@ -574,10 +663,14 @@ cudaError_t launch_stream_m(const GemvParams& p, cudaStream_t s, bool* launched)
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    int sms = 0;
+    int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_stream_kernel<F, M, kQuant>, kThreads,
+                                                          smem)) != cudaSuccess)
+        return e;
+    // two CTAs a SM where they fit (m <= 4), one with the larger staged activations of 8 or 16 tokens
     const int groups = static_cast<int>(p.n / kRows);
-    const int grid = std::max(1, std::min(groups, 2 * sms));   // two CTAs a SM
+    const int grid = std::max(1, std::min(groups, std::min(2, std::max(1, per_sm)) * sms));
     *launched = true;
     return launch_pdl(gemv_stream_kernel<F, M, kQuant>, dim3(grid), dim3(kThreads), smem, s, p);
 }
@@ -586,14 +679,19 @@ template <class F, bool kQuant>
 cudaError_t launch_stream_any(const GemvParams& p, cudaStream_t s, bool* launched) {
     if (p.m <= 1) return launch_stream_m<F, 1, kQuant>(p, s, launched);
     if (p.m <= 2) return launch_stream_m<F, 2, kQuant>(p, s, launched);
-    return launch_stream_m<F, 4, kQuant>(p, s, launched);
+    if (p.m <= 4) return launch_stream_m<F, 4, kQuant>(p, s, launched);
+    if constexpr (F::kMma && !kQuant) {   // 5..16 tokens, q8 input: the tensor-core form
+        if (p.m <= 8) return launch_stream_m<F, 8, false>(p, s, launched);
+        return launch_stream_m<F, 16, false>(p, s, launched);
+    }
+    return cudaSuccess;   // not this kernel's range: *launched stays false
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_stream(const GemvParams& p, cudaStream_t s, bool* launched) {
     *launched = false;
-    if (p.m < 1 || p.m > 4 || p.n % kRows) return cudaSuccess;
+    if (p.m < 1 || p.m > 16 || p.n % kRows) return cudaSuccess;
     if (p.q6) return p.xf ? launch_stream_any<Q6Stream, true>(p, s, launched)
                           : launch_stream_any<Q6Stream, false>(p, s, launched);
     return p.xf ? launch_stream_any<Q4Stream, true>(p, s, launched)

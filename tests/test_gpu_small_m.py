@@ -1,6 +1,7 @@
 """q4k_gemm for decode-sized batches (1 <= m <= 16 tokens): the CUDA-core
-small-M paths (the streamed kernel for m <= 4, the register-held kernels for
-5 <= m <= 16), compared with the oracle.
+small-M paths (the streamed kernel: dp4a for m <= 4, integer mma.sync for
+5 <= m <= 16 of q8 input when the staged activations fit; the register-held
+kernels otherwise), compared with the oracle.
 
 Same bar as the GEMM: per element |y_gpu - y_oracle| <= 1e-4 * sum_k |w_k a_k|
 (plus one bf16 rounding for bf16 output).  The shapes span one and several
