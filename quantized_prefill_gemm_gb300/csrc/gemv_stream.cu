@@ -215,7 +215,7 @@ struct Q4StreamT {
 #pragma unroll
             for (int t = 0; t < M; ++t) {
                 if (t < m) {
-                    const int4* a = reinterpret_cast<const int4*>(act + static_cast<int64_t>(t) * k + 32 * c);
+                    const int4* a = reinterpret_cast<const int4*>(act + (static_cast<int64_t>(c) * M + t) * 32);
                     const int4 a0 = a[0], a1 = a[1];
                     int Jl = __dp4a(l0, a0.x, 0);
                     int Jh = dp4a_us(h0, a0.y, 0);
@@ -226,7 +226,7 @@ struct Q4StreamT {
                     Jl = __dp4a(l3, a1.z, Jl);
                     Jh = dp4a_us(h3, a1.w, Jh);
                     const int J = Jl + (Jh >> 4);
-                    const float2 s = xs[t * kc + c];   // d_a, d_a * ssum (both exact in fp32)
+                    const float2 s = xs[c * M + t];   // d_a, d_a * ssum (both exact in fp32)
                     P[t] = fmaf(s.x, static_cast<float>(sc * J), P[t]);   // sc * J < 2^22: exact
                     Z[t] = fmaf(s.y, mv, Z[t]);
                 }
@@ -267,10 +267,11 @@ struct Q4StreamT {
             const float m1 = static_cast<float>(sl[kMq + j * kRows + g + 8]);
 #pragma unroll
             for (int mi = 0; mi < kN; ++mi) {
-                const uint2 b = *reinterpret_cast<const uint2*>(act + static_cast<int64_t>(8 * mi + g) * k + 32 * c + 8 * q);
+                const uint2 b = *reinterpret_cast<const uint2*>(act + (static_cast<int64_t>(c) * M + 8 * mi + g) * 32 + 8 * q);
                 int d[4];
                 mma_u8s8(d, a0, a1, a2, a3, b.x, b.y);
-                const float2 s0 = xs[(8 * mi + 2 * q) * kc + c], s1 = xs[(8 * mi + 2 * q + 1) * kc + c];
+                const float4 s01 = *reinterpret_cast<const float4*>(xs + c * M + 8 * mi + 2 * q);   // tokens 2q, 2q + 1
+                const float2 s0 = make_float2(s01.x, s01.y), s1 = make_float2(s01.z, s01.w);
                 // d / 16 = J exactly; sc * J < 2^22
                 P[4 * mi + 0] = fmaf(s0.x, static_cast<float>(sc0 * (d[0] >> 4)), P[4 * mi + 0]);
                 P[4 * mi + 1] = fmaf(s1.x, static_cast<float>(sc0 * (d[1] >> 4)), P[4 * mi + 1]);
@@ -395,7 +396,7 @@ struct Q6Stream {
 #pragma unroll
             for (int t = 0; t < M; ++t) {
                 if (t < m) {
-                    const int4* a = reinterpret_cast<const int4*>(act + static_cast<int64_t>(t) * k + 32 * c);
+                    const int4* a = reinterpret_cast<const int4*>(act + (static_cast<int64_t>(c) * M + t) * 32);
                     const int4 a0 = a[0], a1 = a[1];
                     int J0 = dp4a_us(q[0], a0.x, 0);
                     int J1 = dp4a_us(q[4], a1.x, 0);
@@ -405,7 +406,7 @@ struct Q6Stream {
                     J1 = dp4a_us(q[6], a1.z, J1);
                     J0 = dp4a_us(q[3], a0.w, J0);
                     J1 = dp4a_us(q[7], a1.w, J1);
-                    const float2 s = xs[t * kc + c];
+                    const float2 s = xs[c * M + t];
                     const int xp = __float_as_int(s.y);
                     const int X0 = (xp << 16) >> 16, X1 = xp >> 16;
                     const int I = sc0 * (J0 - 32 * X0) + sc1 * (J1 - 32 * X1);
@@ -432,7 +433,7 @@ __host__ __device__ constexpr int ring_depth() {
 }
 
 // ------------------------------------------------------------- layout --
-struct StreamSmem {   // byte offsets: q8 [m][k], (d_a, d_a*ssum) fp32 [m][kc], row partial sums, ring
+struct StreamSmem {   // byte offsets: q8 [kc][M][32], (d_a, second term) fp32 [kc][M], row partial sums, ring
     size_t act, xs, red, ring, total;
     __host__ __device__ static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
     __host__ __device__ StreamSmem(int mslots, int k, int depth, size_t slot) {
@@ -456,8 +457,11 @@ __device__ __forceinline__ void permute_group(uint32_t lo, uint32_t hi, uint32_t
 // Stage the m x k activations: the q8 SoA copied, or fp32 rows quantized by
 // the q8 rule (a 32-element block per pair of threads); with each block's d_a
 // and either d_a * ssum as fp32 (Q4_K) or the code sums of its two 16-element
-// halves as two int16 in the bits of the second float (Q6_K).
-template <bool kQuant, bool kPermuted, bool kHalfSums>
+// halves as two int16 in the bits of the second float (Q6_K).  Chunk-major
+// (act [kc][M][32 B], xs [kc][M]): the tensor-core form's 8 tokens of a chunk
+// are 256 contiguous bytes (8-byte loads without bank conflicts) and a token
+// pair's scales one 16-byte load.
+template <int M, bool kQuant, bool kPermuted, bool kHalfSums>
 __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, float2* xs) {
     const int kc = p.kc, m = p.m, k = p.k;
     if constexpr (kQuant) {
@@ -498,13 +502,13 @@ __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, flo
                 permute_group(w[2], w[3], w[2], w[3]);
             }
             if (live) {
-                reinterpret_cast<uint4*>(act + static_cast<int64_t>(t) * k + 32 * c)[half] = make_uint4(w[0], w[1], w[2], w[3]);
+                reinterpret_cast<uint4*>(act + (static_cast<int64_t>(c) * M + t) * 32)[half] = make_uint4(w[0], w[1], w[2], w[3]);
                 const float da = __half2float(s.da);
                 if constexpr (kHalfSums) {
-                    reinterpret_cast<int16_t*>(&xs[t * kc + c].y)[half] = static_cast<int16_t>(own);
-                    if (half == 0) xs[t * kc + c].x = da;
+                    reinterpret_cast<int16_t*>(&xs[c * M + t].y)[half] = static_cast<int16_t>(own);
+                    if (half == 0) xs[c * M + t].x = da;
                 } else if (half == 0) {
-                    xs[t * kc + c] = make_float2(da, da * static_cast<float>(sum));
+                    xs[c * M + t] = make_float2(da, da * static_cast<float>(sum));
                 }
             }
         }
@@ -516,22 +520,22 @@ __device__ __forceinline__ void stage_acts(const GemvParams& p, int8_t* act, flo
             if constexpr (kHalfSums) {   // piece j is half j % 2 of chunk j / 2
                 const int hs = __dp4a(static_cast<int>(w.x), 0x01010101, __dp4a(static_cast<int>(w.y), 0x01010101,
                                __dp4a(static_cast<int>(w.z), 0x01010101, __dp4a(static_cast<int>(w.w), 0x01010101, 0))));
-                reinterpret_cast<int16_t*>(&xs[t * kc + (j >> 1)].y)[j & 1] = static_cast<int16_t>(hs);
+                reinterpret_cast<int16_t*>(&xs[(j >> 1) * M + t].y)[j & 1] = static_cast<int16_t>(hs);
             }
             if constexpr (kPermuted) {
                 permute_group(w.x, w.y, w.x, w.y);
                 permute_group(w.z, w.w, w.z, w.w);
             }
-            reinterpret_cast<uint4*>(act + static_cast<int64_t>(t) * k)[j] = w;
+            reinterpret_cast<uint4*>(act + (static_cast<int64_t>(j >> 1) * M + t) * 32)[j & 1] = w;
         }
         for (int i = threadIdx.x; i < m * kc; i += kThreads) {
             const int t = i / kc, c = i - t * kc;
             const float da = __half2float(__ushort_as_half(__ldg(p.da + t * kc + c)));
             if constexpr (kHalfSums) {
-                xs[t * kc + c].x = da;
+                xs[c * M + t].x = da;
             } else {
                 const float ss = static_cast<float>(__ldg(p.ssum + t * kc + c));
-                xs[t * kc + c] = make_float2(da, da * ss);
+                xs[c * M + t] = make_float2(da, da * ss);
             }
         }
     }
@@ -584,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
     };
 #pragma unroll 1
     for (int s = 0; s < R - 1; ++s) issue();
-    stage_acts<kQuant, F::kPermuted, F::kHalfSums>(p, act, reinterpret_cast<float2*>(smem_raw + L.xs));
+    stage_acts<M, kQuant, F::kPermuted, F::kHalfSums>(p, act, reinterpret_cast<float2*>(smem_raw + L.xs));
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = threadIdx.x & 15;
