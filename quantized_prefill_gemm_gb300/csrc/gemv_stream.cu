@@ -686,7 +686,20 @@ cudaError_t launch_stream_any(const GemvParams& p, cudaStream_t s, bool* launche
     if (p.m <= 4) return launch_stream_m<F, 4, kQuant>(p, s, launched);
     if constexpr (F::kMma && !kQuant) {   // 5..16 tokens, q8 input: the tensor-core form
         if (p.m <= 8) return launch_stream_m<F, 8, false>(p, s, launched);
-        return launch_stream_m<F, 16, false>(p, s, launched);
+        cudaError_t e = launch_stream_m<F, 16, false>(p, s, launched);
+        if (e != cudaSuccess || *launched) return e;
+        // 16 tokens of a long k do not fit: tokens 0-7, then the rest, each a
+        // pass over the weights (measured: faster than the register-held kernel)
+        GemvParams lo = p, hi = p;
+        lo.m = 8;
+        hi.m = p.m - 8;
+        hi.q8 = p.q8 + 8 * p.ldq;
+        hi.da = p.da + 8 * static_cast<int64_t>(p.kc);
+        hi.ssum = p.ssum + 8 * static_cast<int64_t>(p.kc);
+        hi.y = p.out_bf16 ? static_cast<void*>(static_cast<__nv_bfloat16*>(p.y) + 8 * p.ldy)
+                          : static_cast<void*>(static_cast<float*>(p.y) + 8 * p.ldy);
+        if ((e = launch_stream_m<F, 8, false>(lo, s, launched)) != cudaSuccess || !*launched) return e;
+        return launch_stream_m<F, 8, false>(hi, s, launched);
     }
     return cudaSuccess;   // not this kernel's range: *launched stays false
 }

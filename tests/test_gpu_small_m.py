@@ -76,13 +76,16 @@ def test_decode_sizes(q4k, n, k, m, out):
 
 
 @pytest.mark.parametrize("n,k,m,out", [(4096, 11008, 1, "bf16"), (12288, 4096, 1, "bf16"),
-                                       (22016, 4096, 1, "bf16"), (128, 256, 2, "f32"), (640, 2304, 3, "f32")])
+                                       (22016, 4096, 1, "bf16"), (128, 256, 2, "f32"), (640, 2304, 3, "f32"),
+                                       (640, 2304, 6, "f32"), (4096, 11008, 16, "bf16"), (512, 11008, 12, "f32")])
 def test_streamed_shapes(q4k, n, k, m, out):
-    """Shapes that exercise the streamed kernel (m <= 4) in particular, every
-    output checked: the 7B down projection (43 super-blocks, so each group
-    ends with a stage of 3), q|k|v and gate|up stored as one matrix (768 and
-    1376 16-row groups: several per CTA), a single super-block (a one-super-
-    block stage), and 40 groups with 9 super-blocks (a short second stage)."""
+    """Shapes that exercise the streamed kernel in particular, every output
+    checked: the 7B down projection (43 super-blocks, so each group ends with
+    a stage of 3), q|k|v and gate|up stored as one matrix (768 and 1376
+    16-row groups: several per CTA), a single super-block (a one-super-block
+    stage), 40 groups with 9 super-blocks (a short second stage), and the
+    tensor-core form with 6 tokens and with 12 and 16 tokens of k = 11008
+    (too many staged activations for one pass: two passes of 8 tokens)."""
     _check(q4k, n, k, m, "silu_mul" if k >= 11008 else "normal", 90 + m, out=out)
 
 
