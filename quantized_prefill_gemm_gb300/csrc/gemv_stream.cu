@@ -98,6 +98,14 @@ __device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, 
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0), "r"(0), "r"(0), "r"(0));
 }
 
+// The same with k = 16 (m16n8k16): lane l holds A rows l/4 and l/4 + 8 at
+// k-slots 4(l%4)..+3 (a0, a1) and B column l/4 at the same slots (b0).
+__device__ __forceinline__ void mma_u8s8_k16(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%9,%10};"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(a0), "r"(a1), "r"(b0), "r"(0), "r"(0), "r"(0), "r"(0));
+}
+
 // Q6_K quants q = u ^ 32 (0..63, unsigned bytes) of one packed 8-k group from
 // its low-nibble word and its 2-bit high fields hf (at the group's nibble
 // positions, low two bits of each nibble), in the two permuted byte orders
@@ -119,6 +127,7 @@ struct Q4StreamT {
     static constexpr bool kPermuted = true;   // activations staged in the nibble order
     static constexpr bool kHalfSums = false;  // staged: d_a * ssum
     static constexpr bool kMma = true;        // 8 and 16 tokens on the tensor cores (compute_mma)
+    static constexpr int kMmaChunks = 8;      // chunks a warp takes per stage in that form: one super-block
     static constexpr uint32_t kNib = 0;
     static constexpr uint32_t kSc = kNib + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kMq = kSc + 8 * kStageSb * kRows;
@@ -305,7 +314,8 @@ struct Q6Stream {
     static constexpr int kItems = 2;
     static constexpr bool kPermuted = true;
     static constexpr bool kHalfSums = true;   // staged: the two half-chunk code sums
-    static constexpr bool kMma = false;
+    static constexpr bool kMma = true;        // 8 and 16 tokens on the tensor cores (compute_mma)
+    static constexpr int kMmaChunks = 4;      // chunks a warp takes per stage in that form: half a super-block
     static constexpr uint32_t kLo = 0;
     static constexpr uint32_t kHi = kLo + 8 * kStageSb * kRows * 16;
     static constexpr uint32_t kSc = kHi + 8 * kStageSb * kRows * 8;
@@ -417,6 +427,73 @@ struct Q6Stream {
         const float d = reinterpret_cast<const float*>(sl + kD)[(j0 >> 3) * kRows + r];
 #pragma unroll
         for (int t = 0; t < M; ++t) acc[t] = fmaf(d, P[t], acc[t]);
+    }
+    // 8 or 16 tokens on the tensor cores: warp w takes chunks 4w..4w+3 of the
+    // stage (half of super-block w/2) for all 16 rows, two m16n8k16 MMAs per
+    // chunk, one per 16-weight half (its own scale).  The A operand is the
+    // unsigned q = u ^ 32: for half h, k-slots 4i..4i+3 hold word 2h + i/2 of
+    // the row in the low-nibble (i even) or high-nibble (i odd) byte order of
+    // the Q4_K masks; B is the activations staged in the same order.  Then
+    // I = sc_h * (D_h - 32 X_h) summed over the halves, exact.
+    // acc[4 mi + e]: rows l/4 (e < 2) and l/4 + 8, tokens 8 mi + 2(l%4) + e%2.
+    template <int M>
+    __device__ static void compute_mma(const uint8_t* sl, int w, int lane, int c0, const int8_t* act, const float2* xs,
+                                       int k, int kc, float (&acc)[M / 2]) {
+        constexpr int kN = M / 8;
+        const int g = lane >> 2, q = lane & 3;
+        const int wq = q >> 1;            // this lane's word within a half
+        const bool odd = (q & 1) != 0;    // high-nibble byte order
+        float P[4 * kN];
+#pragma unroll
+        for (int i = 0; i < 4 * kN; ++i) P[i] = 0.0f;
+#pragma unroll 2
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * w + jj, c = c0 + jj;
+            uint32_t a[2][2];   // [half][row g, row g + 8]
+            int sc[2][2];       // [row][half]
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = g + 8 * rr;
+                const uint32_t* lw = reinterpret_cast<const uint32_t*>(sl + kLo + (j * kRows + row) * 16);
+                const uint2 hw = *reinterpret_cast<const uint2*>(sl + kHi + (j * kRows + row) * 8);
+                const uint32_t scp = *reinterpret_cast<const uint16_t*>(sl + kSc + (j * kRows + row) * 2);
+                sc[rr][0] = static_cast<int>(static_cast<int8_t>(scp & 0xFFu));
+                sc[rr][1] = static_cast<int>(static_cast<int8_t>(scp >> 8));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t q0, q1;
+                    q6_bytes(lw[2 * h + wq], (h ? hw.y : hw.x) >> (2 * wq), q0, q1);
+                    a[h][rr] = odd ? q1 : q0;
+                }
+            }
+#pragma unroll
+            for (int mi = 0; mi < kN; ++mi) {
+                const int8_t* bt = act + (static_cast<int64_t>(c) * M + 8 * mi + g) * 32 + 4 * q;
+                int d0[4], d1[4];
+                mma_u8s8_k16(d0, a[0][0], a[0][1], *reinterpret_cast<const uint32_t*>(bt));
+                mma_u8s8_k16(d1, a[1][0], a[1][1], *reinterpret_cast<const uint32_t*>(bt + 16));
+                const float4 s01 = *reinterpret_cast<const float4*>(xs + c * M + 8 * mi + 2 * q);   // tokens 2q, 2q + 1
+                const int xp0 = __float_as_int(s01.y), xp1 = __float_as_int(s01.w);
+                const int x00 = (xp0 << 16) >> 16, x01 = xp0 >> 16, x10 = (xp1 << 16) >> 16, x11 = xp1 >> 16;
+                P[4 * mi + 0] = fmaf(s01.x, static_cast<float>(sc[0][0] * (d0[0] - 32 * x00) + sc[0][1] * (d1[0] - 32 * x01)),
+                                     P[4 * mi + 0]);
+                P[4 * mi + 1] = fmaf(s01.z, static_cast<float>(sc[0][0] * (d0[1] - 32 * x10) + sc[0][1] * (d1[1] - 32 * x11)),
+                                     P[4 * mi + 1]);
+                P[4 * mi + 2] = fmaf(s01.x, static_cast<float>(sc[1][0] * (d0[2] - 32 * x00) + sc[1][1] * (d1[2] - 32 * x01)),
+                                     P[4 * mi + 2]);
+                P[4 * mi + 3] = fmaf(s01.z, static_cast<float>(sc[1][0] * (d0[3] - 32 * x10) + sc[1][1] * (d1[3] - 32 * x11)),
+                                     P[4 * mi + 3]);
+            }
+        }
+        const float* dv = reinterpret_cast<const float*>(sl + kD) + (w >> 1) * kRows;
+        const float dg0 = dv[g], dg1 = dv[g + 8];
+#pragma unroll
+        for (int mi = 0; mi < kN; ++mi) {
+            acc[4 * mi + 0] = fmaf(dg0, P[4 * mi + 0], acc[4 * mi + 0]);
+            acc[4 * mi + 1] = fmaf(dg0, P[4 * mi + 1], acc[4 * mi + 1]);
+            acc[4 * mi + 2] = fmaf(dg1, P[4 * mi + 2], acc[4 * mi + 2]);
+            acc[4 * mi + 3] = fmaf(dg1, P[4 * mi + 3], acc[4 * mi + 3]);
+        }
     }
 };
 
@@ -593,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = threadIdx.x & 15;
     const int j0 = (threadIdx.x >> 4) * F::kItems;   // this thread's first chunk in a stage
-    constexpr bool kMma = M >= 8;                     // tensor-core form: warp w takes super-block w of a stage
+    constexpr bool kMma = M >= 8;                     // tensor-core form: warp w takes F::kMmaChunks chunks of a stage
     constexpr int kAcc = kMma ? M / 2 : M;
     float acc[kAcc];
 #pragma unroll
@@ -607,7 +684,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const GemvPara
         const int nch = 8 * min(kSb, ksb - sb0);
         const uint8_t* sl = smem_raw + L.ring + static_cast<size_t>(slot) * F::kSlot;
         if constexpr (kMma) {
-            if (8 * warp < nch) F::template compute_mma<M>(sl, warp, lane, 8 * (sb0 + warp), act, xs, k, kc, acc);
+            if (F::kMmaChunks * warp < nch)
+                F::template compute_mma<M>(sl, warp, lane, 8 * sb0 + F::kMmaChunks * warp, act, xs, k, kc, acc);
         } else {
             if (j0 < nch) F::template compute<M>(sl, j0, r, 8 * sb0 + j0, act, xs, m, k, kc, acc);
         }

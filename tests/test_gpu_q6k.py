@@ -63,10 +63,13 @@ def test_decode_sizes(q4k, n, k, m, out):
     _check(q4k, n, k, m, 50 + m, out=out, kind="silu_mul" if k == 11008 else "normal")
 
 
-@pytest.mark.parametrize("n,k,m,out", [(4096, 11008, 1, "bf16"), (128, 256, 2, "f32"), (640, 2304, 3, "f32")])
+@pytest.mark.parametrize("n,k,m,out", [(4096, 11008, 1, "bf16"), (128, 256, 2, "f32"), (640, 2304, 3, "f32"),
+                                       (640, 2304, 6, "f32"), (512, 11008, 12, "bf16"), (11008, 4096, 8, "bf16")])
 def test_streamed_shapes(q4k, n, k, m, out):
-    """Shapes of the streamed small-M kernel (m <= 4): 43 super-blocks (a short
-    last stage of 3), one super-block, 9 super-blocks over 40 row groups."""
+    """Shapes of the streamed small-M kernel: 43 super-blocks (a short last
+    stage of 3), one super-block, 9 super-blocks over 40 row groups; the
+    tensor-core form with 6 and 8 tokens, and 12 tokens of k = 11008 (two
+    passes of 8 tokens)."""
     _check(q4k, n, k, m, 55 + m, out=out, kind="silu_mul" if k == 11008 else "normal")
 
 
