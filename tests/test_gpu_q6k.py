@@ -168,3 +168,10 @@ def test_prefill_extreme_scales_exact(q4k):
     assert np.array_equal(acc.cpu().numpy().astype(np.int64), ints)
     want, scale = _oracle(blocks, x)
     assert_close(y.float().cpu().double().numpy(), want, scale, "f32", "q6k extreme scales")
+
+
+def test_long_k_takes_the_register_held_kernel(q4k):
+    """k = 20480 with 8 tokens: beyond the streamed kernel's shared memory, the
+    register-held Q6_K kernel takes it; every output checked."""
+    _check(q4k, 128, 20480, 8, 140, out="f32", act="q8")
+

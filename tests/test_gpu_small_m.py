@@ -189,3 +189,12 @@ def test_in_kernel_quantization_strided_rows_and_no_workspace(q4k):
     torch.cuda.synchronize()
     want, scale = oracle_rows(blocks, x, np.arange(m))
     assert_close(y.cpu().double().numpy(), want, scale, "f32", "strided fp32 rows, no workspace")
+
+
+@pytest.mark.parametrize("m", [2, 8])
+def test_long_k_takes_the_register_held_kernels(q4k, m):
+    """k = 20480 with 8 tokens stages more activations than the streamed
+    kernel holds: the register-held kernels take it (and m = 2 the streamed
+    one); every output checked."""
+    _check(q4k, 128, 20480, m, "normal", 130 + m, out="f32", act="q8")
+
