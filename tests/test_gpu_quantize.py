@@ -80,17 +80,25 @@ def test_q8_strided_rows(q4k):
     assert np.array_equal(ss.cpu().numpy(), wss)
 
 
-def test_act_operand_layout(q4k):
+@pytest.mark.parametrize("m,k,ld", [
+    (200, 512, 512),      # 16 blocks a token: whole warps
+    (130, 768, 768),      # 24 blocks: the second warp of a token holds 8
+    (3, 11008, 11264),    # 344 blocks (21.5 warps), strided rows
+    (1, 256, 256),        # one 8-block token, 127 padding tokens
+])
+def test_act_operand_layout(q4k, m, k, ld):
     """The GEMM operand form in the workspace: fp16 qa, fp32 d_a per 128-token
-    tile, and d_a*ssum split into two bf16 planes (hi + lo)."""
+    tile (zero for the padding tokens), and d_a*ssum split into two bf16 planes
+    (hi + lo)."""
     from quantized_prefill_gemm_gb300 import inputs
 
-    from tests.gpu_common import to_dev
+    from tests.gpu_common import DEV, to_dev
 
-    m, k = 200, 512
     kc = k // 32
     x = inputs.activations(m, k, 7, "outlier")
-    ws = q4k.q4k_act_quantize(to_dev(x)).cpu().numpy()
+    big = torch.full((m, ld), float("nan"), dtype=torch.float32, device=DEV)
+    big[:, :k] = to_dev(x)
+    ws = q4k.q4k_act_quantize(big[:, :k]).cpu().numpy()
     wq, wda, wss = oq8.quantize_rows(x)
     da = wda.view(np.float16).astype(np.float32)
     align = lambda v: (v + 1023) // 1024 * 1024
