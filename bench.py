@@ -359,6 +359,10 @@ def main():
     ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS) + ["peak_s8"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quant", default="pass", choices=["pass", "inkernel"],
+                    help="prefill from fp32: a separate quantization pass before each GEMM (q4k_act_quantize + "
+                         "q4k_gemm_quantized, the q4k_gemm path) or the GEMM kernel quantizing x itself "
+                         "(q4k_gemm_inkernel_quant)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
@@ -412,6 +416,8 @@ def main():
     if tokens <= 16:   # decode-sized: the small-M path
         return run_decode(args, q4k, torch, dev, dist, world, rank, local, packed, mats, xs, ys, ws, stream)
 
+    inkernel = args.quant == "inkernel" and q8in is None and not q6
+
     def step(events=None):
         for i, (n, k) in enumerate(mats):
             if q6:   # q6k_gemm quantizes into ws (fp16 operand) and runs the GEMM: the events take both
@@ -419,13 +425,19 @@ def main():
                     events[i][0].record(stream)
                 q4k.q6k_gemm(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws, stream=stream)
             else:
-                if q8in is not None:   # the q8 SoA -> the GEMM's operand form
-                    q4k.q4k_act_from_q8(*q8in[i], workspace=ws, stream=stream)
+                if inkernel:   # one launch: the GEMM kernel quantizes x (the events take all of it)
+                    if events is not None:
+                        events[i][0].record(stream)
+                    q4k.q4k_gemm_inkernel_quant(packed[i], n, k, xs[i], out_dtype=out, y=ys[i], workspace=ws,
+                                                stream=stream)
                 else:
-                    q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
-                if events is not None:
-                    events[i][0].record(stream)
-                q4k.q4k_gemm_quantized(packed[i], n, k, ws, tokens, out, y=ys[i], stream=stream)
+                    if q8in is not None:   # the q8 SoA -> the GEMM's operand form
+                        q4k.q4k_act_from_q8(*q8in[i], workspace=ws, stream=stream)
+                    else:
+                        q4k.q4k_act_quantize(xs[i], workspace=ws, stream=stream)
+                    if events is not None:
+                        events[i][0].record(stream)
+                    q4k.q4k_gemm_quantized(packed[i], n, k, ws, tokens, out, y=ys[i], stream=stream)
             if events is not None:
                 events[i][1].record(stream)
 
@@ -484,7 +496,7 @@ def main():
             e2e = run_e2e_q8(q4k, torch, dev, packed, mats, tokens, out, q8in, ws, stream)
         else:
             e2e = run_e2e(q4k, torch, dev, packed, mats, tokens, out, xs, ws, stream,
-                          gemm=q4k.q6k_gemm if q6 else None)
+                          gemm=q4k.q6k_gemm if q6 else q4k.q4k_gemm_inkernel_quant if inkernel else None)
 
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -493,6 +505,9 @@ def main():
                       else "f16 x f16 -> f32 tensor-core MMA on exact q4/q8 integers"),
             "data": "synthetic (seeded random {} weights and activations)".format("Q6_K" if q6 else "Q4_K"),
             "config": {"workload": desc, "tokens": tokens, "gemms_per_step": len(mats),
+                       "quantization": ("in the GEMM kernel (q4k_gemm_inkernel_quant)" if inkernel else
+                                        "q8 SoA converted by q4k_act_from_q8" if q8in is not None else
+                                        "separate pass (q4k_act_quantize), as q4k_gemm runs it"),
                        "l2": (f"L2 flushed before each timed step ({FLUSH_BYTES >> 20} MB written outside the step's "
                               f"events): a step touches only {(wb + xb + yb) / 1e6:.0f} MB" if flush is not None else
                               f"inputs larger than L2 (a step touches {(wb + xb + yb) / 1e9:.2f} GB)"),
@@ -504,7 +519,8 @@ def main():
                             "step time: distance from the HBM limit of a tensor-bound path".format(
                                 210 if q6 else 144, "q8 SoA" if q8in is not None else "fp32")),
             "clocks": clk,
-            "gpu_launches": sum(gemm_launches(tokens, n, k, sms) for n, k in mats) * args.steps}
+            "gpu_launches": sum(gemm_launches(tokens, n, k, sms) - (1 if inkernel else 0) for n, k in mats)
+            * args.steps}
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:

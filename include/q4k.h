@@ -160,6 +160,38 @@ q4k_status q4k_gemm_quantized(const void* packed_w, int64_t n, int64_t k,
                               void* y, int out_dtype, int64_t ldy, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * q4k_gemm_inkernel_quant -- q4k_gemm for fp32 activations in one kernel
+ * launch: the GEMM kernel quantizes x into `workspace` itself ("34 · r31 --
+ * q-major sda scale-read repack", §1 for the q8 blocks; the same operation
+ * order as q4k_act_quantize, so the operand bits are the same).  Its warps
+ * with no other work at that moment quantize: the tiles the first wave of
+ * output tiles reads before it starts, the rest while the tiles run; a
+ * 128-token tile's product starts once every slice of it is quantized (the
+ * CTAs wait for one another, so the kernel is a cooperative launch: it
+ * fails with Q4K_ERR_CUDA rather than starting when the GPU cannot hold all
+ * of its CTAs at once).  On a GB300 it measured 5-7% slower than q4k_gemm's
+ * separate quantization pass (512 to 2630 tokens, 4096-11008 features),
+ * which is why q4k_gemm does not take this path.
+ *   packed_w, n, k, y, out_dtype, ldy: as q4k_gemm.
+ *   x [m][ldx] fp32, 16-byte aligned, ldx % 4 == 0, ldx >= k; m >= 0 (the
+ *   tensor-core GEMM for every m, no small-M path).
+ *   workspace: >= q4k_act_workspace_bytes(m, k) bytes, 256-byte aligned; on
+ *   return its operand part holds what q4k_act_quantize would write.  It also
+ *   holds one 64-bit counter per 128-token tile, tagged with the call: the
+ *   workspace needs no initialisation (a call never mistakes an earlier
+ *   call's counts, or leftover bytes, for its own unless they happen to hold
+ *   this call's 48-bit tag), and calls that may overlap in time must not
+ *   share it.
+ *   Output: identical bits to q4k_act_quantize + q4k_gemm_quantized except
+ *   where the two split different output tiles along k to balance the last
+ *   wave (this call orders the tiles output-tile first), where the fp32 sums
+ *   are added in another order; the accuracy contract is q4k_gemm's.
+ * ------------------------------------------------------------------------ */
+q4k_status q4k_gemm_inkernel_quant(const void* packed_w, int64_t n, int64_t k, const float* x, int64_t m,
+                                   int64_t ldx, void* y, int out_dtype, int64_t ldy,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Gate/up pair with a SiLU(gate)*up epilogue that produces the down
  * projection's quantized input.  The pages measure LLaMA-7B's linear layers
  * ("34 · r31 — q-major sda scale-read repack", Result: 7B q4_K whole-prefill);

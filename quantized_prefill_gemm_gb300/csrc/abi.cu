@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -108,6 +110,19 @@ q4k_status encode_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* b
     return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
+// The tag of one GEMM call that quantizes its activations in the kernel: a
+// fixed mark in bits 48-63 and a per-process call counter in bits 16-47 (bits
+// 0-15 carry the kernel's counts).  The counter starts at a clock-derived
+// value, so that a count another process left in reused memory is unlikely to
+// carry the same tag either.
+unsigned long long next_quant_tag() {
+    static std::atomic<uint32_t> counter{
+        static_cast<uint32_t>(static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) *
+                              2654435761ull)};
+    const uint32_t e = counter.fetch_add(1u, std::memory_order_relaxed);
+    return (0x51A4ull << 48) | (static_cast<unsigned long long>(e) << 16);
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int64_t kMaxDim = int64_t(1) << 31;
@@ -138,9 +153,12 @@ q4k_status check_output(const void* y, int64_t m, int64_t n, int out, int64_t ld
 // h_ws (gate/up pair weights only): instead of Y, write the down projection's
 // operand of SiLU(gate)*up, ActLayout(m, n / 2), there; y, out and ldy are then
 // unused.  The caller has checked h_ws.  q6: Q6_K weights (Q6Layout); the
-// activation operand in ws has the same fp16 form as for Q4_K.
+// activation operand in ws has the same fp16 form as for Q4_K.  xf: fp32
+// activations [m][ldx] (checked by the caller) that the GEMM kernel quantizes
+// into ws itself; without it ws already holds the operand.
 q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t ws_bytes, int64_t m, void* y,
-                    int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream, bool q6 = false) {
+                    int out, int64_t ldy, float* dbg, void* h_ws, cudaStream_t stream, bool q6 = false,
+                    const float* xf = nullptr, int64_t ldx = 0) {
     q4k_status st = check_gemm_shape(n, k, m);
     if (st != Q4K_OK) return st;
     if (!h_ws && (st = check_output(y, m, n, out, ldy)) != Q4K_OK) return st;
@@ -232,6 +250,24 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
         p.hkc = static_cast<int>(n / 64);
     }
     const int grid = std::min(p.num_units, dev->sm_count);
+    if (xf) {   // in-kernel quantization (gemm.cu): items of the operand, counted per token tile
+        p.nt_fast = 1;   // output tiles fastest: the first wave reads the first token tiles only
+        p.xf = xf;
+        p.ldx = ldx;
+        p.xq_w = reinterpret_cast<uint16_t*>(ab + A.xq);
+        p.da_w = reinterpret_cast<float*>(ab + A.da);
+        p.e_w = reinterpret_cast<__nv_bfloat16*>(ab + A.e);
+        p.qflag = reinterpret_cast<unsigned long long*>(ab + A.flag);
+        p.qtag = next_quant_tag();
+        // the last token tile the first wave of units reads; its tiles and the
+        // ones before it are cut into about one item per CTA
+        const int last = std::min(grid, p.num_units) - 1;
+        const int tile = last < p.full_tiles ? last : p.full_tiles + (last - p.full_tiles) / p.split;
+        const int mt1 = tile / p.n_tiles;
+        p.qs = std::max(1, std::min(p.kc, grid / (mt1 + 1)));
+        p.q_items = p.m_tiles * p.qs;
+        p.q_early = std::min(p.q_items, (mt1 + 1) * p.qs);
+    }
     if ((st = from_cuda(launch_gemm(tm_x, tm_e, tm_d, p, grid, stream))) != Q4K_OK) return st;
     return p.split > 1 ? from_cuda(launch_split_fixup(p, stream)) : Q4K_OK;
 }
@@ -447,6 +483,19 @@ q4k_status q4k_gemm(const void* packed_w, int64_t n, int64_t k, int act, const v
     }
     if (st != Q4K_OK) return st;
     return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream);
+}
+
+q4k_status q4k_gemm_inkernel_quant(const void* packed_w, int64_t n, int64_t k, const float* x, int64_t m,
+                                   int64_t ldx, void* y, int out_dtype, int64_t ldy, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+    q4k_status st = check_gemm_shape(n, k, m);
+    if (st != Q4K_OK) return st;
+    if ((st = check_output(y, m, n, out_dtype, ldy)) != Q4K_OK) return st;
+    if ((st = check_act_f32(x, m, k, ldx)) != Q4K_OK) return st;
+    if (!packed_w) return Q4K_ERR_INVALID_ARG;
+    if (!aligned(packed_w, 256)) return Q4K_ERR_ALIGNMENT;
+    return run_gemm(packed_w, n, k, workspace, workspace_bytes, m, y, out_dtype, ldy, nullptr, nullptr, stream, false,
+                    x, ldx);
 }
 
 q4k_status q4k_gemm_swiglu(const void* packed_pair, int64_t n, int64_t k, int act, const void* x_or_q8,

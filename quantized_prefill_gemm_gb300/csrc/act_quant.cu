@@ -20,6 +20,7 @@
 #include "q4k_internal.h"
 #include "q4k_layout.h"
 #include "q4k_ptx.cuh"
+#include "q8_operand.cuh"
 #include "q8_rule.cuh"
 
 namespace q4k {
@@ -94,14 +95,6 @@ __device__ __forceinline__ BlockQ8 quantize_block(const float* __restrict__ src)
     return b;
 }
 
-// E = d_a * ssum (exact in fp32: an 11-bit by <= 12-bit product) split into
-// two bf16 terms hi + lo with |E - hi - lo| <= 2^-16 |E|.
-__device__ __forceinline__ void split_e(__half da, int ssum, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-    const float e = __fmul_rn(__half2float(da), static_cast<float>(ssum));
-    hi = __float2bfloat16_rn(e);
-    lo = __float2bfloat16_rn(__fsub_rn(e, __bfloat162float(hi)));
-}
-
 // Public SoA output, 8-lane groups (small batches).
 __global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_lanes_kernel(const float* __restrict__ x, int64_t m,
                                                                          int64_t k, int64_t ldx,
@@ -159,12 +152,6 @@ __global__ void __launch_bounds__(kThreadsPerBlock) q8_rows_kernel(const float* 
     ssum[t * kc + c] = static_cast<int16_t>(b.ssum);
 }
 
-// Two q8 codes as an exact fp16 pair (the GEMM operand of both weight formats).
-__device__ __forceinline__ uint32_t code_pair(int q0, int q1) {
-    const __half2 pr = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-    return *reinterpret_cast<const uint32_t*>(&pr);
-}
-
 __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64_t m, int64_t k, int64_t kc,
                                               const int (&q)[4], __half da, int ssum, uint16_t* __restrict__ xq,
                                               float* __restrict__ dat, __nv_bfloat16* __restrict__ e) {
@@ -182,8 +169,9 @@ __device__ __forceinline__ void write_operand(int64_t t, int64_t c, int j, int64
 }
 
 // GEMM operand form (see q4k_layout.h; fp16 codes) from fp32 activations.  A
-// lane pair takes one 32-k block (16 values a lane, its four 16-B loads in
-// flight together; amax and ssum need one shuffle), and a warp 16 consecutive
+// lane pair takes one 32-k block (quantize_pair_block in q8_operand.cuh, the
+// routine the GEMM's in-kernel quantization runs too: 16 values a lane, its
+// four 16-B loads in flight together; amax and ssum need one shuffle), and a warp 16 consecutive
 // blocks of one token (2 KB of fp32; k is a multiple of 256, so the last warp
 // of a token may hold 8).  Against an 8-lane group per block this halves the
 // shuffles and doubles the bytes each lane has in flight: 12% less time at
@@ -200,48 +188,8 @@ __global__ void __launch_bounds__(kThreadsPerBlock) act_quant_kernel(const float
     const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t t = wid / wpt, c = (wid % wpt) * 16 + (lane >> 1);
-    const int half = lane & 1;   // which 16 values of block c
-    if (t >= mp) return;         // whole warps: t is the same across the warp
-    const bool live = c < kc;    // both lanes of a pair agree
-    if (t >= m) {                // padding token of the last 128-token tile: scale 0
-        if (live && half == 0) dat[((t >> 7) * kc + c) * 128 + (t & 127)] = 0.0f;
-        return;
-    }
-    const float4* src = reinterpret_cast<const float4*>(x + t * ldx + (live ? c : 0) * 32 + 16 * half);
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 f = live ? __ldcs(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[4 * i] = f.x;
-        v[4 * i + 1] = f.y;
-        v[4 * i + 2] = f.z;
-        v[4 * i + 3] = f.w;
-    }
-    float amax = fabsf(v[0]);
-#pragma unroll
-    for (int i = 1; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-    const Q8Scale sc = q8_scale(amax);
-    uint32_t w[8];
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int q0 = q8_code(v[2 * i], sc), q1 = q8_code(v[2 * i + 1], sc);
-        sum += q0 + q1;
-        w[i] = code_pair(q0, q1);
-    }
-    sum += __shfl_xor_sync(kFull, sum, 1);
-    if (!live) return;
-    uint4* dst = reinterpret_cast<uint4*>(xq + t * k + c * 32 + 16 * half);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    if (half == 0) {
-        dat[((t >> 7) * kc + c) * 128 + (t & 127)] = __half2float(sc.da);
-        __nv_bfloat16 hi, lo;
-        split_e(sc.da, sum, hi, lo);
-        e[t * kc + c] = hi;
-        e[(m + t) * kc + c] = lo;
-    }
+    if (t >= mp) return;   // whole warps: t is the same across the warp
+    quantize_pair_block(x, ldx, m, k, kc, t, c, lane & 1, c < kc, xq, dat, e);
 }
 
 // GEMM operand form from the public q8 SoA ([m][ldq] int8, da, ssum [m][kc]).

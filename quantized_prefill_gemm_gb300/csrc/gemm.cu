@@ -47,6 +47,7 @@
 #include "q4k_layout.h"
 #include "q4k_ptx.cuh"
 #include "q4k_unpack.cuh"
+#include "q8_operand.cuh"
 #include "q8_rule.cuh"
 
 namespace q4k {
@@ -93,7 +94,7 @@ struct Lay {
     static constexpr int kBarDFull = kBarDrain + 1;          // [kDRing] producer -> drain (tx bytes)
     static constexpr int kBarDEmpty = kBarDFull + kDRing;    // [kDRing] 8 drain warps -> producer
     static constexpr int kNumBars = kBarDEmpty + kDRing;
-    static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag
+    static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;   // TMEM base slot, abort flag, ready unit
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
     static constexpr size_t kSmemBytes = kSmemUsed + 1024;          // + alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -112,7 +113,8 @@ constexpr uint32_t kIdescMin = idesc_kind_f16(128, 128, true);     // bf16 x bf1
 // used: the running Y left TMEM, and with it the MMA's wait for a free Y)
 enum : unsigned {
     kSiteProdEmpty = 1, kSiteUnused2, kSiteMmaFull, kSiteMmaConv, kSiteMmaAccEmpty,
-    kSiteConvFull, kSiteEpiD, kSiteEpiAccFull, kSiteEpiZ, kSiteProdD
+    kSiteConvFull, kSiteEpiD, kSiteEpiAccFull, kSiteEpiZ, kSiteProdD,
+    kSiteProdQuant, kSiteEpiReady, kSiteQuantArrive
 };
 
 template <bool kQ6>
@@ -122,6 +124,7 @@ struct Ctx {
     uint8_t* sbase;     // generic pointer to the same
     uint32_t tmem;      // TMEM base address (lane 0, column 0)
     volatile int* abort_flag;
+    uint32_t ready;     // shared address of the ready-unit word (in-kernel quantization)
     __device__ uint32_t bar(int i) const { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); }
     __device__ uint32_t a(int s) const { return base + L::kOffA + L::kStageA * s; }
     __device__ uint32_t b(int s) const { return base + L::kOffB + L::kStageB * s; }
@@ -183,13 +186,119 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
         w.kbase = kb0 - zst;
         w.n_st = zst + kb1 - kb0;
     }
-    w.mt = tile % p.m_tiles;
-    w.nt = tile / p.m_tiles;
+    if (p.nt_fast) {
+        w.nt = tile % p.n_tiles;
+        w.mt = tile / p.n_tiles;
+    } else {
+        w.mt = tile % p.m_tiles;
+        w.nt = tile / p.m_tiles;
+    }
     return w;
 }
 
+// ------------------------------------------------ in-kernel quantization --
+// With x given in fp32 the kernel writes the activation operand itself, with
+// the routine of the separate pass (quantize_pair_block), so the bits are the
+// same.  The work is cut into items, (token tile, slice of its kc blocks),
+// qs slices a tile.  A CTA's items are done by warps that have nothing else
+// to do at that moment: the items the first wave of tiles needs by the eight
+// drain warps before their first accumulator, the rest by the two spare
+// warps while the tiles run.  With the output tile fastest in the tile order
+// the first wave needs only the first ceil(grid / n_tiles) token tiles.  A
+// finished item adds one to its token tile's count, tagged with the call so
+// that counts of an earlier call on the same workspace are never mistaken
+// for this one's; the producer waits for a full count (qs items) before the
+// first copy of a unit's activation tiles and tells the drain (which reads
+// d_a with plain loads) through a ready word in shared memory.
+
+// Item `it` with `nw` warps (this one is number qw): passes of 16 * kR
+// (token, block) pairs a warp, each lane with the loads of kR pairs in flight.
+template <int kR>
+__device__ __forceinline__ void quantize_item(const GemmParams& p, int it, int nw, int qw, int lane) {
+    const int mt = it / p.qs, j = it - mt * p.qs;
+    const int c0 = static_cast<int>(static_cast<int64_t>(j) * p.kc / p.qs);
+    const int nb = static_cast<int>(static_cast<int64_t>(j + 1) * p.kc / p.qs) - c0;
+    const int pairs = 128 * nb;
+    for (int base = 16 * kR * qw; base < pairs; base += 16 * kR * nw) {
+        float v[kR][16];
+        int64_t t[kR], c[kR];
+        bool in[kR];
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+            const int q = base + 16 * r + (lane >> 1);
+            in[r] = q < pairs;
+            const int tt = in[r] ? q / nb : 0;
+            t[r] = static_cast<int64_t>(mt) * 128 + tt;
+            c[r] = c0 + (in[r] ? q - tt * nb : 0);
+            pair_load(p.xf, p.ldx, p.m, t[r], c[r], lane & 1, in[r], v[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < kR; ++r)
+            pair_finish(v[r], p.m, p.k, p.kc, t[r], c[r], lane & 1, in[r], p.xq_w, p.da_w, p.e_w);
+    }
+}
+
+// One item of token tile mt finished (the caller has ordered every write of
+// it before this thread, by a barrier): release it into the tile's count.  The
+// first arrival of a call finds the word under another tag (an earlier call's,
+// or whatever the workspace held) and installs this call's with a count of
+// one; every other arrival adds one.  Only this call writes the word while it
+// runs, so the exchange is retried at most once (after losing the
+// installation to another arrival of this call); the additions queue in L2
+// instead of retrying round trips.
+__device__ __forceinline__ void quantize_arrive(const GemmParams& p, int mt) {
+    fence_proxy_async_global();
+    fence_acq_rel_gpu();
+    unsigned long long* f = p.qflag + mt;
+    unsigned long long cur = ld_relaxed_gpu_u64(f);
+    for (int i = 0; i < 4; ++i) {
+        if ((cur & ~0xFFFFull) == p.qtag) {
+            atomicAdd(f, 1ull);
+            return;
+        }
+        const unsigned long long prev = atomicCAS(f, cur, p.qtag | 1ull);
+        if (prev == cur) return;
+        cur = prev;
+    }
+    atomicCAS(p.err, 0u, kErrTimeoutBase | kSiteQuantArrive);
+}
+
+// Items it0, it0 + gridDim.x, ... below it_end with the nw warps that call
+// this together (named barrier `bar`; warp number qw among them).
+template <int kR>
+__device__ __forceinline__ void quantize_items(const GemmParams& p, int it0, int it_end, int nw, int qw, int lane,
+                                               uint32_t bar) {
+    for (int it = it0; it < it_end; it += gridDim.x) {
+        quantize_item<kR>(p, it, nw, qw, lane);
+        fence_proxy_async_global();   // the writes, for the other CTAs' tensor copies
+        named_bar_sync(bar, 32u * static_cast<uint32_t>(nw));
+        if (qw == 0 && lane == 0) quantize_arrive(p, it / p.qs);
+    }
+}
+
+// The producer's wait for a full count of token tile mt, then the acquire.
+__device__ __forceinline__ bool quantize_wait(const GemmParams& p, int mt, volatile int* abort) {
+    const unsigned long long want = p.qtag | static_cast<unsigned long long>(p.qs);
+    const unsigned long long* f = p.qflag + mt;
+    if (ld_relaxed_gpu_u64(f) != want) {
+        const long long t0 = clock64();
+        while (ld_relaxed_gpu_u64(f) != want) {
+            __nanosleep(100);
+            if (*abort) return false;
+            if (static_cast<uint64_t>(clock64() - t0) > p.timeout_cycles) {
+                atomicCAS(p.err, 0u, kErrTimeoutBase | kSiteProdQuant);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    fence_acq_rel_gpu();          // the items' writes happen before what follows
+    fence_proxy_async_global();   // including the tensor copies of the activation tiles
+    return true;
+}
+
 // ------------------------------------------------------------- producer --
-template <bool kQ6>
+template <bool kQ6, bool kQuant>
 __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParams& p, const CUtensorMap* tm_x,
                                              const CUtensorMap* tm_e, const CUtensorMap* tm_d) {
     using L = Lay<kQ6>;
@@ -197,9 +306,20 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
     uint32_t ph = 0, issued = 0, parity_bits = 0;
     uint32_t dph = 0, d_issued = 0, d_parity_bits = 0;
     bool ok = true;
+    int ready_mt = -1;   // token tile whose operand this thread has seen complete
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = unit_of<kQ6>(p, u);
         const int mt = w.mt, nt = w.nt;
+        if constexpr (kQuant) {   // the operand of tile mt is written by this kernel
+            if (mt != ready_mt) {
+                if (!quantize_wait(p, mt, cx.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ready_mt = mt;
+            }
+            st_release_cta_u32(cx.ready, static_cast<uint32_t>(u) + 1u);   // for the drain's d_a loads
+        }
         for (int st = 0; st < w.n_st; ++st) {
             if (!cx.wait(p, L::kBarEmpty + s, ph ^ 1u, kSiteProdEmpty)) {
                 ok = false;
@@ -602,13 +722,46 @@ __device__ __forceinline__ void store_partial(const GemmParams& p, const float* 
     for (int i = 0; i < 16; ++i) dst[i] = make_float4(Y[4 * i], Y[4 * i + 1], Y[4 * i + 2], Y[4 * i + 3]);
 }
 
+// d_a: through the read-only path when another kernel wrote it, through L2
+// when this kernel did (the read-only path keeps no promise for data written
+// while the kernel runs).
+template <bool kQuant>
+__device__ __forceinline__ float load_da(const float* a) {
+    if constexpr (kQuant) return __ldcg(a);
+    return __ldg(a);
+}
+
+// The drain's wait for the producer's word that unit `want - 1` has its
+// operand complete (every lane polls; the word only grows).
+template <bool kQ6>
+__device__ __forceinline__ bool ready_wait(const Ctx<kQ6>& cx, const GemmParams& p, uint32_t want) {
+    bool ok = true;
+    if (ld_acquire_cta_u32(cx.ready) < want) {
+        const long long t0 = clock64();
+        while (ld_acquire_cta_u32(cx.ready) < want) {
+            __nanosleep(64);
+            if (*cx.abort_flag) {
+                ok = false;
+                break;
+            }
+            if (static_cast<uint64_t>(clock64() - t0) > p.timeout_cycles) {
+                atomicCAS(p.err, 0u, kErrTimeoutBase | kSiteEpiReady);
+                *cx.abort_flag = 1;
+                ok = false;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Drain warp e (0..7) reads TMEM lanes 32*(warp%4)..+31 (the lane quadrant
 // its warp index allows) and columns 64*(e/4)..+63 of each accumulator: each
 // thread owns one token row and 64 output columns.  Per main stage it folds
 // both chunks, P += d_a * J (packed fp32 FMA), and hands the group back after
 // its last TMEM load; per super-block Y += d * P, with d from the d ring
 // (it never waits on or releases a stage of the main ring); per unit Y -> HBM.
-template <bool kDump, bool kSwiGLU, bool kQ6>
+template <bool kDump, bool kSwiGLU, bool kQ6, bool kQuant>
 __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParams& p, int warp, int e, int lane) {
     using L = Lay<kQ6>;
     const int qd = warp & 3, ch = e >> 2;
@@ -635,11 +788,17 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
         constexpr int kDaAhead = 3;
         const int c_end = L::kCh * (w.kbase + w.n_st);
         const float* dap = p.da + static_cast<int64_t>(mt) * p.kc * 128 + row;   // + 128 * chunk
+        if constexpr (kQuant) {
+            if (!ready_wait(cx, p, static_cast<uint32_t>(u) + 1u)) {
+                ok = false;
+                break;
+            }
+        }
         float dq[2 * kDaAhead];
         {
             const int c0 = L::kCh * max(w.kbase, 0);
 #pragma unroll
-            for (int i = 0; i < 2 * kDaAhead; ++i) dq[i] = c0 + i < c_end ? __ldg(dap + 128 * (c0 + i)) : 0.0f;
+            for (int i = 0; i < 2 * kDaAhead; ++i) dq[i] = c0 + i < c_end ? load_da<kQuant>(dap + 128 * (c0 + i)) : 0.0f;
         }
         for (int st = 0; st < w.n_st; ++st) {
             const int kb = st + w.kbase;
@@ -673,8 +832,8 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
 #pragma unroll
                     for (int i = 0; i + 2 < 2 * kDaAhead; ++i) dq[i] = dq[i + 2];
                     if (c + 2 * kDaAhead < c_end) {
-                        dq[2 * kDaAhead - 2] = __ldg(dap + 128 * (c + 2 * kDaAhead));
-                        dq[2 * kDaAhead - 1] = __ldg(dap + 128 * (c + 2 * kDaAhead + 1));
+                        dq[2 * kDaAhead - 2] = load_da<kQuant>(dap + 128 * (c + 2 * kDaAhead));
+                        dq[2 * kDaAhead - 1] = load_da<kQuant>(dap + 128 * (c + 2 * kDaAhead + 1));
                     }
                     if (!cx.warp_wait(p, L::kBarAccFull + g, gph, kSiteEpiAccFull)) {
                         ok = false;
@@ -760,7 +919,8 @@ __device__ __forceinline__ void run_epilogue(const Ctx<kQ6>& cx, const GemmParam
 // kSwiGLU: gate/up pair weights; the tile end writes the down projection's
 // q8 operand of SiLU(gate)*up instead of Y.
 // kQ6: Q6_K weights (Q6Layout), two fp16 weight planes per stage.
-template <bool kDump, bool kSwiGLU, bool kQ6>
+// kQuant: fp32 activations (p.xf), quantized into the workspace by the kernel.
+template <bool kDump, bool kSwiGLU, bool kQ6, bool kQuant>
 __global__ void __launch_bounds__(kThreads, 1)
     q4k_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_e,
                     const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
@@ -772,6 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.base = base;
     cx.sbase = smem_raw + (base - raw);
     cx.abort_flag = reinterpret_cast<volatile int*>(cx.sbase + L::kOffMisc + 4);
+    cx.ready = base + L::kOffMisc + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     griddep_launch_dependents();
 
@@ -791,6 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(cx.bar(L::kBarDrain), 1);
         *cx.abort_flag = 0;
+        *reinterpret_cast<volatile uint32_t*>(cx.sbase + L::kOffMisc + 8) = 0u;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(base + L::kOffMisc, 512);
@@ -813,18 +975,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         regs_dec<kRegsCtl>();
         if (warp == 0) {
-            if (lane == 0) run_producer<kQ6>(cx, p, &tm_x, &tm_e, &tm_d);
+            if (lane == 0) run_producer<kQ6, kQuant>(cx, p, &tm_x, &tm_e, &tm_d);
             __syncwarp();
         } else if (warp == 1) {
             if (lane == 0) run_mma<kQ6>(cx, p);
             __syncwarp();
-        }   // warps 2 and 3 have no role
+        } else if constexpr (kQuant) {   // warps 2 and 3: the items the first wave does not need
+            quantize_items<1>(p, p.q_early + (blockIdx.x + gridDim.x - p.q_early % gridDim.x) % gridDim.x,
+                              p.q_items, 2, warp - 2, lane, 2u);
+        }
     } else if (warp < 8) {
         regs_dec<kRegsConv>();
         run_converter<kQ6>(cx, p, warp - 4, lane);
     } else {
         regs_inc<kRegsDrain>();
-        run_epilogue<kDump, kSwiGLU, kQ6>(cx, p, warp, warp - 8, lane);
+        // the first wave's items, before the first accumulator can arrive
+        if constexpr (kQuant) quantize_items<4>(p, blockIdx.x, p.q_early, 8, warp - 8, lane, 1u);
+        run_epilogue<kDump, kSwiGLU, kQ6, kQuant>(cx, p, warp, warp - 8, lane);
     }
 
     tc_fence_before();
@@ -853,7 +1020,8 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
     const int64_t tail = gid >> 12;
     if (tail >= p.num_tiles - p.full_tiles) return;
     const int tile = p.full_tiles + static_cast<int>(tail);
-    const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    const int mt = p.nt_fast ? tile / p.n_tiles : tile % p.m_tiles;
+    const int nt = p.nt_fast ? tile % p.n_tiles : tile / p.m_tiles;
     const int64_t t = static_cast<int64_t>(mt) * 128 + (e >> 1) * 32 + r;
     if (t >= p.m) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -889,7 +1057,8 @@ __global__ void __launch_bounds__(256) split_fixup_swiglu_kernel(const GemmParam
     const int64_t tail = wid >> 8;
     if (tail >= p.num_tiles - p.full_tiles) return;
     const int tile = p.full_tiles + static_cast<int>(tail);
-    const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    const int mt = p.nt_fast ? tile / p.n_tiles : tile % p.m_tiles;
+    const int nt = p.nt_fast ? tile % p.n_tiles : tile / p.m_tiles;
     const int64_t t = static_cast<int64_t>(mt) * 128 + (e >> 1) * 32 + r;
     const int c = 2 * nt + (e & 1);
     if (t >= p.m) {   // padding token of the last 128-token tile: scale 0
@@ -948,7 +1117,7 @@ __global__ void selftest_wait_kernel(unsigned* err, uint64_t timeout_cycles) {
     __syncthreads();
 }
 
-template <bool kDump, bool kSwiGLU, bool kQ6>
+template <bool kDump, bool kSwiGLU, bool kQ6, bool kQuant>
 cudaError_t launch_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                            const GemmParams& p, int grid, cudaStream_t s) {
     static std::atomic<bool> attr_set[64];   // zero at start; a race only repeats the call
@@ -958,12 +1127,16 @@ cudaError_t launch_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_e, con
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     constexpr size_t smem = Lay<kQ6>::kSmemBytes;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(q4k_gemm_kernel<kDump, kSwiGLU, kQ6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+        e = cudaFuncSetAttribute(q4k_gemm_kernel<kDump, kSwiGLU, kQ6, kQuant>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(q4k_gemm_kernel<kDump, kSwiGLU, kQ6>, dim3(grid), dim3(kThreads), smem, s, tm_x, tm_e, tm_d, p);
+    // in-kernel quantization: CTAs wait for items other CTAs quantize, so all
+    // of them must be resident together (a cooperative launch, refused rather
+    // than started if they cannot be)
+    return launch_pdl_coop(q4k_gemm_kernel<kDump, kSwiGLU, kQ6, kQuant>, kQuant, dim3(grid), dim3(kThreads), smem, s,
+                           tm_x, tm_e, tm_d, p);
 }
 
 }  // namespace
@@ -971,12 +1144,16 @@ cudaError_t launch_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_e, con
 cudaError_t launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_e, const CUtensorMap& tm_d,
                         const GemmParams& p, int grid, cudaStream_t s) {
     if (p.hq && (p.dbg || p.q6)) return cudaErrorInvalidValue;
+    if (p.xf) {   // in-kernel quantization: plain Q4_K weights only
+        if (p.dbg || p.q6 || p.hq) return cudaErrorInvalidValue;
+        return launch_variant<false, false, false, true>(tm_x, tm_e, tm_d, p, grid, s);
+    }
     if (p.q6)
-        return p.dbg ? launch_variant<true, false, true>(tm_x, tm_e, tm_d, p, grid, s)
-                     : launch_variant<false, false, true>(tm_x, tm_e, tm_d, p, grid, s);
-    if (p.hq) return launch_variant<false, true, false>(tm_x, tm_e, tm_d, p, grid, s);
-    return p.dbg ? launch_variant<true, false, false>(tm_x, tm_e, tm_d, p, grid, s)
-                 : launch_variant<false, false, false>(tm_x, tm_e, tm_d, p, grid, s);
+        return p.dbg ? launch_variant<true, false, true, false>(tm_x, tm_e, tm_d, p, grid, s)
+                     : launch_variant<false, false, true, false>(tm_x, tm_e, tm_d, p, grid, s);
+    if (p.hq) return launch_variant<false, true, false, false>(tm_x, tm_e, tm_d, p, grid, s);
+    return p.dbg ? launch_variant<true, false, false, false>(tm_x, tm_e, tm_d, p, grid, s)
+                 : launch_variant<false, false, false, false>(tm_x, tm_e, tm_d, p, grid, s);
 }
 
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s) {

@@ -27,6 +27,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The same, and with `coop` also as a cooperative launch: every CTA of the
+// grid is resident at once, or the launch fails.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), bool coop, dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = coop ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // 32-k chunks per main stage of the tensor-core GEMM: 4 (128 k) for Q4_K,
 // 2 (64 k) for Q6_K, whose stages carry two fp16 weight planes.
 __host__ __device__ constexpr int gemm_chunks_per_stage(bool q6) { return q6 ? 2 : 4; }
@@ -62,6 +82,24 @@ struct GemmParams {
     // dsb = d) with the fp16 activation operand; no min term
     const uint8_t* q6hi;    // the high quant bits [nt][kc][128][8 B]
     int q6;
+    // Tile order: 0 = token tile fastest (tile = nt * m_tiles + mt), 1 = output
+    // tile fastest (tile = mt * n_tiles + nt), the order the in-kernel
+    // quantization needs (the first wave then reads the first token tiles only).
+    int nt_fast;
+    // In-kernel quantization (xf set): the kernel writes the activation operand
+    // (xq, da, e of the workspace) from fp32 x itself.  Item i = (token tile
+    // i / qs, slice i % qs of its kc blocks); item i is quantized by CTA
+    // i % gridDim.x, items below q_early at the start by the drain warps, the
+    // others alongside the GEMM by the two spare warps.  qflag[mt] counts the
+    // finished items of token tile mt under this call's tag qtag.
+    const float* xf;        // [m][ldx] fp32, or null (operand already in the workspace)
+    int64_t ldx;
+    uint16_t* xq_w;         // the workspace's xq, da and e, written by the kernel
+    float* da_w;
+    __nv_bfloat16* e_w;
+    unsigned long long* qflag;   // [m_tiles]
+    unsigned long long qtag;     // bits 16-63; the count lives in bits 0-15
+    int qs, q_early, q_items;
 };
 
 cudaError_t launch_q8_quantize_rows(const float* x, int64_t m, int64_t k, int64_t ldx, int8_t* q8,

@@ -24,6 +24,10 @@
 //   part [kMaxSplitUnits][8][32][64] f32  partial tiles of the GEMM's k-split
 //                                 tail: unit (tail tile, part), slice (2 x row
 //                                 quadrant + column half), row, column
+//   flag [mp/128]          u64   in-kernel quantization (q4k_gemm from fp32):
+//                                 per 128-token tile, the call's tag in bits
+//                                 16-63 and the count of its quantized slices
+//                                 in bits 0-15 (gemm.cu)
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
@@ -74,14 +78,15 @@ struct Q6Layout {
 };
 
 struct ActLayout {
-    int64_t xq, da, e, part, total;
+    int64_t xq, da, e, part, flag, total;
     ActLayout(int64_t m, int64_t k) {
         const int64_t kc = k / 32, mp = align_up(m, kTileM);
         xq = 0;
         da = align_up(xq + m * k * 2, kAlign);
         e = align_up(da + mp * kc * 4, kAlign);
         part = align_up(e + 2 * m * kc * 2, kAlign);
-        total = align_up(part + kMaxSplitUnits * 8 * 32 * 64 * 4, kAlign);
+        flag = align_up(part + kMaxSplitUnits * 8 * 32 * 64 * 4, kAlign);
+        total = align_up(flag + (mp / kTileM) * 8, kAlign);
     }
 };
 

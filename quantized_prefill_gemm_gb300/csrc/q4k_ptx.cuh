@@ -311,4 +311,32 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
                  : "memory");
 }
 
+// ------------------------------------------- flags between CTAs of one grid
+// A flag written by one CTA and read by another: the writer releases
+// (fence, then a relaxed atomic), the reader polls with relaxed loads and
+// acquires with a fence once it has seen the value.  Memory a TMA (the async
+// proxy) reads after such an acquire also needs the proxy fence, on both sides.
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Within a CTA: a shared-memory word one thread publishes and others poll.
+__device__ __forceinline__ void st_release_cta_u32(uint32_t saddr, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta_u32(uint32_t saddr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+    return v;
+}
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 }  // namespace q4k

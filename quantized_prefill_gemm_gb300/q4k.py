@@ -40,6 +40,8 @@ SIGNATURES = {
     "q4k_act_from_q8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr, _c_size, _c_ptr]),
     "q4k_gemm_quantized": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_size, _c_i64, _c_ptr, _c_int, _c_i64,
                                     _c_ptr]),
+    "q4k_gemm_inkernel_quant": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_int, _c_i64,
+                                         _c_ptr, _c_size, _c_ptr]),
     "q4k_device_error_word": (_c_uint, [_c_int]),
     "q4k_device_status": (_c_int, [_c_int]),
     "q4k_selftest_wait_timeout": (_c_int, [_c_i64, _c_ptr]),
@@ -213,6 +215,20 @@ def q4k_gemm(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, out_dtype="f
         _dev(da, "da", torch.float16) if act == ACT_Q8 else None,
         _dev(ssum, "ssum", torch.int16) if act == ACT_Q8 else None,
         m, ldx, _dev(y, "y"), code, ldy, _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return y
+
+
+def q4k_gemm_inkernel_quant(packed: torch.Tensor, n: int, k: int, x: torch.Tensor, out_dtype="f32", y=None,
+                            workspace=None, stream=None) -> torch.Tensor:
+    """q4k_gemm for fp32 x in one launch: the GEMM kernel quantizes x itself."""
+    m, kx, ldx = _row_major(x, "x")
+    if kx != k:
+        raise ValueError("x has the wrong number of columns")
+    code, y, ldy = _out(m, n, out_dtype, y, x.device)
+    workspace = _workspace(q4k_act_workspace_bytes(m, k), x.device, workspace)
+    _check("q4k_gemm_inkernel_quant", LIB.q4k_gemm_inkernel_quant(
+        _dev(packed, "packed"), n, k, _dev(x, "x", torch.float32), m, ldx, _dev(y, "y"), code, ldy,
+        _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
     return y
 
 

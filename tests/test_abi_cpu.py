@@ -95,6 +95,18 @@ def test_host_validation_rejects_before_any_cuda_call(q4k):
     assert gemm(m=32, act=1, ws_bytes=16) == 1
     assert gemm(act=1) == 1              # q8 input without da / ssum
     assert gemm(m=0) == 0                # empty batch is a no-op
+    # q4k_gemm_inkernel_quant: shapes, output, activation stride, workspace size, empty batch
+    def inkernel(n=256, k=512, m=8, ldx=512, out=0, ldy=256, ws_bytes=1 << 30, x=args["x"]):
+        return L.q4k_gemm_inkernel_quant(args["w"], n, k, x, m, ldx, args["y"], out, ldy, args["ws"], ws_bytes, null)
+
+    assert inkernel(n=200) == 2
+    assert inkernel(k=300) == 2
+    assert inkernel(out=4) == 1
+    assert inkernel(ldx=500) == 2
+    assert inkernel(x=null) == 1
+    assert inkernel(x=ctypes.c_void_p(4100)) == 3
+    assert inkernel(ws_bytes=16) == 4
+    assert inkernel(m=0) == 0
     # debug hook size limit
     assert L.q4k_gemm_debug_chunk_acc(args["w"], 128 * 64, 4096, args["ws"], 1 << 30, 4096, args["y"], 8192,
                                       ctypes.c_void_p(4096), null) == 2
