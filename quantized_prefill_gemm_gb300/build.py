@@ -7,6 +7,7 @@ so a stale binary is never picked up after a header edit.
 from __future__ import annotations
 
 import hashlib
+import re
 import os
 import shutil
 import subprocess
@@ -48,13 +49,27 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def _local_includes(src: str) -> list:
+    """src and every file of this directory it includes, directly or not
+    (#include "name" lines), in a fixed order."""
+    seen, todo = [], [src]
+    while todo:
+        f = todo.pop(0)
+        if f in seen or not os.path.exists(os.path.join(CSRC, f)):
+            continue
+        seen.append(f)
+        with open(os.path.join(CSRC, f)) as fh:
+            todo += re.findall(r'^\s*#include\s+"([^"/]+)"', fh.read(), flags=re.M)
+    return seen
+
+
 def gemm_digest() -> str:
     """Hash of what the tensor-core GEMM kernel is built from: gemm.cu, the
     headers it includes, and the flags.  Measurements of that kernel (the
     per-shape DRAM traffic table under profiles/) are keyed by it, so they
     stay valid while other kernels change."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "q4k_internal.h", "q4k_layout.h", "q4k_ptx.cuh", "q4k_unpack.cuh", "q8_rule.cuh"):
+    for f in _local_includes("gemm.cu"):
         h.update(f.encode())
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
