@@ -49,30 +49,39 @@ def _digest() -> str:
     return h.hexdigest()
 
 
-def _local_includes(src: str) -> list:
-    """src and every file of this directory it includes, directly or not
+def _local_includes(src: str, csrc: str = CSRC) -> list:
+    """src and every file of the directory csrc it includes, directly or not
     (#include "name" lines), in a fixed order."""
     seen, todo = [], [src]
     while todo:
         f = todo.pop(0)
-        if f in seen or not os.path.exists(os.path.join(CSRC, f)):
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
             continue
         seen.append(f)
-        with open(os.path.join(CSRC, f)) as fh:
+        with open(os.path.join(csrc, f)) as fh:
             todo += re.findall(r'^\s*#include\s+"([^"/]+)"', fh.read(), flags=re.M)
     return seen
 
 
-def gemm_digest() -> str:
-    """Hash of what the tensor-core GEMM kernel is built from: gemm.cu, the
-    headers it includes, and the flags.  Measurements of that kernel (the
-    per-shape DRAM traffic table under profiles/) are keyed by it, so they
-    stay valid while other kernels change."""
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank space (a comment edit does
+    not change the kernel)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def gemm_digest(csrc: str = CSRC) -> str:
+    """Hash of what the tensor-core GEMM kernel is built from: the code of
+    gemm.cu and of the headers it includes (comments left out), and the
+    flags.  Measurements of that kernel (the per-shape DRAM traffic table
+    under profiles/) are keyed by it, so they stay valid while other kernels,
+    or only comments, change."""
     h = hashlib.sha256()
-    for f in _local_includes("gemm.cu"):
+    for f in _local_includes("gemm.cu", csrc):
         h.update(f.encode())
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     h.update(" ".join(ARCH + [c for c in CFLAGS if not c.startswith("-I")]).encode())
     return h.hexdigest()
 

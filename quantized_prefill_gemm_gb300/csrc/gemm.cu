@@ -28,12 +28,15 @@
 //   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk, two chunks into
 //                 the two accumulators of one TMEM group, one commit for both;
 //                 4 bf16 MMAs per 64 of min-term depth into a group's first one
-//   warps 2-3     no role (they complete the first warpgroup)
+//   warps 2-3     no role (they complete the first warpgroup); with the
+//                 in-kernel quantization (kQuant) they quantize the
+//                 activation items the first wave of tiles does not need
 //   warps 4-7     converters: 4-bit quants -> fp16 sc*q written in the
 //                 128-B-swizzled K-major layout the MMA reads
 //   warps 8-15    drain: per chunk, P += da * J (packed fp32 FMA) from TMEM;
 //                 per super-block Y += d * P; per tile Y -> HBM.  Y and P live
-//                 in registers (setmaxnreg gives these warps 184 each).
+//                 in registers (setmaxnreg gives these warps 184 each).  With
+//                 kQuant they first quantize the first wave's items.
 // TMEM (512 columns): two groups of two 128-column accumulators.  A group is
 // handed over once per two chunks, which halves the MMA <-> drain hand-offs
 // of a per-chunk scheme; those hand-offs, not the tensor pipe, bound the loop.
