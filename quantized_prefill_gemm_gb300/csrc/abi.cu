@@ -225,7 +225,9 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     // writes each part's partial tile to the workspace; a small kernel then
     // adds a tile's parts in part order (deterministic) and finishes the tile
     // as usual, so Y, or the SiLU(gate)*up operand, comes from the same fp32
-    // sums whichever output the call asks for.
+    // sums whichever output the call asks for.  Tiles of fewer than four
+    // super-blocks are not split: the fixup launch costs more than the
+    // shorter units save (measured: 256 x 512 at 64 tokens, 18.0 -> 15.8 us).
     p.split = 1;
     p.part_sb = p.ksb;
     p.full_tiles = p.num_tiles;
@@ -233,7 +235,7 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     const int rem = p.num_tiles % sms;
     if (rem > 0) {
         const int parts = std::min(sms / rem, p.ksb);
-        if (parts >= 2) {
+        if (parts >= 2 && p.ksb >= 4) {
             p.part_sb = (p.ksb + parts - 1) / parts;
             p.split = (p.ksb + p.part_sb - 1) / p.part_sb;
             p.full_tiles = p.num_tiles - rem;

@@ -42,7 +42,8 @@ def test_step_footprint_qproj_and_ffn_configs():
     (2048, 4096, 11008, 3),    # 512 tiles, split 2 ways (43 super-blocks)
     (512, 4096, 4096, 2),      # 128 tiles: one partial wave that cannot split (152 // 128 = 1)
     (2432, 4096, 4096, 2),     # 19 x 32 = 608 tiles: exactly 4 waves, nothing left over
-    (256, 1024, 512, 3),       # 16 tiles, split min(152 // 16, 2) = 2 ways
+    (256, 1024, 1024, 3),      # 16 tiles, split min(152 // 16, 4) = 4 ways
+    (256, 1024, 512, 2),       # two super-blocks: not split (the fixup would cost more than it saves)
     (256, 1024, 256, 2),       # one super-block: no split possible
 ])
 def test_gemm_launches(m, n, k, want):

@@ -45,7 +45,7 @@ def _ws(q4k, m, k, fill):
 
 
 CASES = [
-    (200, 256, 512, "f32"),      # 2 token tiles, k-split tail, every item at the start
+    (200, 256, 1024, "f32"),     # 2 token tiles, k-split tail, every item at the start
     (300, 11008, 4096, "bf16"),  # 86 output tiles: the first wave reads 2 of 3 token tiles
     (130, 4096, 11008, "f32"),   # 344 blocks in 64 slices of 5 or 6
     (2048, 256, 4096, "f32"),    # 16 token tiles, 4-way k-split
