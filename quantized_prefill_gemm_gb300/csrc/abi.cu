@@ -214,9 +214,8 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     p.m_tiles = static_cast<int>((m + kTileM - 1) / kTileM);
     p.n_tiles = static_cast<int>(n / kTileN);
     p.num_tiles = p.m_tiles * p.n_tiles;
-    // min-term stages: three hi/lo parts per depth block of one stage's chunks
-    const int64_t zdepth = 32 * gemm_chunks_per_stage(q6);
-    p.n_zst = q6 ? 0 : static_cast<int>(3 * ((kc + zdepth - 1) / zdepth));
+    // min-term stages: one per 64 of depth (hi and lo of both operands)
+    p.n_zst = q6 ? 0 : static_cast<int>((kc + 63) / 64);
     p.n_main = static_cast<int>(k / (32 * gemm_chunks_per_stage(q6)));
     p.out_bf16 = out == Q4K_OUT_BF16 ? 1 : 0;
     // Tail balance: after the last full wave of tiles over the SMs, the R

@@ -27,7 +27,8 @@
 //                 own; for the min-term stages the bf16 E and -(dmin*m) tiles
 //   warp 1        MMA issuer: 2 x (M128 N128 K16) per chunk, two chunks into
 //                 the two accumulators of one TMEM group, one commit for both;
-//                 4 bf16 MMAs per 64 of min-term depth into a group's first one
+//                 12 bf16 MMAs per 64 of min-term depth (hi*hi, hi*lo, lo*hi)
+//                 into a group's first one
 //   warps 2-3     no role (they complete the first warpgroup); with the
 //                 in-kernel quantization (kQuant) they quantize the
 //                 activation items the first wave of tiles does not need
@@ -63,7 +64,8 @@ constexpr int kThreads = 512;
 // quants and sc.  Q6_K: four stages of 64 k (the B tile has two fp16
 // planes, the sh and the sl part of the scale) plus the high quant bits.  A and B tiles are made of
 // 16 KB boxes of 128 rows x 64 k (128-B rows, 128-B swizzle), one per two
-// chunks.  A min-term stage uses as many boxes of A and B, each 64 deep.
+// chunks.  A min-term stage holds 64 of depth: the hi and the lo box of E in
+// the A slots, those of -(dmin*m) in the B slots (Q4_K only).
 // The super-block scales d have a ring of their own, shared by the producer
 // and the drain only, so that the drain (the slowest role) never holds a
 // stage of the main ring.
@@ -338,15 +340,19 @@ __device__ __forceinline__ void run_producer(const Ctx<kQ6>& cx, const GemmParam
             }
             const uint32_t fb = cx.bar(L::kBarFull + s);
             if (st + w.kbase < 0) {
-                // min-term stage: depth block j (32 kCh chunks of the rank-kc
-                // product, one box of 64 per two) of hi/lo part `part`
-                const int j = st / 3, part = st - 3 * j;   // part 0: hi*hi, 1: hi*lo, 2: lo*hi
-                mbar_arrive_expect_tx(fb, 2 * L::kBox * (L::kCh / 2));
-#pragma unroll
-                for (int i = 0; i < L::kCh / 2; ++i) {   // boxes wholly past kc read zeros
-                    const int x = 32 * L::kCh * j + 64 * i;
-                    tma_load_3d(cx.a(s) + L::kBox * i, tm_e, fb, x, 128 * mt, part == 2 ? 1 : 0);
-                    tma_load_3d(cx.b(s) + L::kBox * i, tm_d, fb, x, 128 * nt, part == 1 ? 1 : 0);
+                if constexpr (!kQ6) {
+                    // min-term stage st: depth block st (64 chunks of the
+                    // rank-kc product) of E hi and lo into the two A boxes and
+                    // of -(dmin*m) hi and lo into the two B boxes, so that the
+                    // three products hi*hi, hi*lo and lo*hi come from one load
+                    // of each (a box partly past kc reads zeros there)
+                    static_assert(L::kStageA >= 2 * L::kBox && L::kStageB >= 2 * L::kBox, "min-term boxes");
+                    const int x = 64 * st;
+                    mbar_arrive_expect_tx(fb, 4 * L::kBox);
+                    tma_load_3d(cx.a(s), tm_e, fb, x, 128 * mt, 0);
+                    tma_load_3d(cx.a(s) + L::kBox, tm_e, fb, x, 128 * mt, 1);
+                    tma_load_3d(cx.b(s), tm_d, fb, x, 128 * nt, 0);
+                    tma_load_3d(cx.b(s) + L::kBox, tm_d, fb, x, 128 * nt, 1);
                 }
             } else {
                 const int kb = kb_;
@@ -422,14 +428,17 @@ __device__ __forceinline__ void run_mma(const Ctx<kQ6>& cx, const GemmParams& p)
             }
             tc_fence_after();
             if (kb < 0) {
-                const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
-#pragma unroll
-                for (int i = 0; i < L::kCh / 2; ++i) {
-                    const uint64_t ad = sw128_kmajor_desc(cx.a(s) + L::kBox * i);
-                    const uint64_t bd = sw128_kmajor_desc(cx.b(s) + L::kBox * i);
+                if constexpr (!kQ6) {   // hi*hi, hi*lo and lo*hi over the block's 64 of depth
+                    const uint32_t tg = cx.tmem + 256u * static_cast<uint32_t>(g);
+                    const uint64_t ah = sw128_kmajor_desc(cx.a(s)), al = sw128_kmajor_desc(cx.a(s) + L::kBox);
+                    const uint64_t bh = sw128_kmajor_desc(cx.b(s)), bl = sw128_kmajor_desc(cx.b(s) + L::kBox);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)   // K = 64 in four K16 steps of 32 B
-                        tc_mma_f16(tg, ad + 2u * kk, bd + 2u * kk, kIdescMin, (st | i | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16(tg, ah + 2u * kk, bh + 2u * kk, kIdescMin, (st | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tg, ah + 2u * kk, bl + 2u * kk, kIdescMin, 1u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tg, al + 2u * kk, bh + 2u * kk, kIdescMin, 1u);
                 }
                 tc_commit(cx.bar(L::kBarEmpty + s));
                 if (kb == -1) {   // Z complete: the group goes to the drain

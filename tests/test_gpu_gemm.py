@@ -204,11 +204,11 @@ def test_k_split_four_parts_ragged_token_tile(q4k):
 
 
 def test_long_k_min_term_boxes_and_exact_chunks(q4k):
-    """K = 14336 (448 chunks): 112 main stages of 128 k and 12 min-term stages,
-    whose last depth block holds one box partly and one wholly past kc (read as
-    zeros); 150 tokens leave the token tile ragged.  Every output against the
-    oracle, and every per-chunk integer exact."""
-    m, n, k = 150, 256, 14336
+    """K = 14080 (440 chunks): 110 main stages of 128 k and 7 min-term stages of
+    64 chunks each, the last holding 56 chunks and reading zeros past kc; 150
+    tokens leave the token tile ragged.  Every output against the oracle, and
+    every per-chunk integer exact."""
+    m, n, k = 150, 256, 14080
     blocks, x = make_case(n, k, m, "outlier", seed=123)
     y = _run(q4k, blocks, x, n, k, "f32")
     want, scale = oracle_rows(blocks, x, np.arange(m))
