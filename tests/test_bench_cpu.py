@@ -78,3 +78,20 @@ def test_clock_record_parsing():
     hot = "1500, 2070, 300.0, 0x8, Not Active, Active, Not Active, Not Active"
     assert bench.ClockSampler.parse(hot)["reasons"] == ["hw_thermal_slowdown"]
     assert bench.ClockSampler.parse("")["sm_mhz"] is None
+
+
+def test_gemm_digest_follows_code_not_comments(tmp_path):
+    """The GEMM traffic table is keyed by a hash of the GEMM's code: the files
+    it includes count, comments and blank space do not."""
+    from quantized_prefill_gemm_gb300 import build
+
+    def write(main, header):
+        (tmp_path / "gemm.cu").write_text('#include "h.cuh"\n' + main)
+        (tmp_path / "h.cuh").write_text(header)
+        return build.gemm_digest(str(tmp_path))
+
+    base = write("int f() { return 1; }  // one\n", "/* a */ int g();\n")
+    assert build._local_includes("gemm.cu", str(tmp_path)) == ["gemm.cu", "h.cuh"]
+    assert write("int f() {\n  return 1;   // another comment\n}\n", "/* b\n c */ int g();\n") == base
+    assert write("int f() { return 2; }\n", "int g();\n") != base
+    assert write("int f() { return 1; }\n", "int g(int);\n") != base
