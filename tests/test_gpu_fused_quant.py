@@ -110,3 +110,22 @@ def test_fused_empty_batch(q4k):
     y = q4k.q4k_gemm_inkernel_quant(packed, n, k, x[:0])   # a no-op
     torch.cuda.synchronize()
     assert y.shape == (0, n)
+
+
+@pytest.mark.parametrize("name", ["qproj512", "qproj2630", "ffn2048"])
+def test_fused_full_size_configs_sampled(q4k, name):
+    """The configurations that take fp32 activations, at full size, through the
+    in-kernel quantization: sampled token rows (tile edges and the ragged tail
+    included) against the oracle, in each configuration's output type."""
+    from tests.gpu_common import CONFIGS, sample_rows
+
+    c = CONFIGS[name]
+    m = c["m"]
+    rows = sample_rows(m, 24, c["seed"])
+    for i, (n, k, kind) in enumerate(c["mats"]):
+        blocks, x = make_case(n, k, m, kind, c["seed"], tag=i)
+        packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
+        y = q4k.q4k_gemm_inkernel_quant(packed, n, k, to_dev(x), out_dtype=c["out"])
+        torch.cuda.synchronize()
+        want, scale = oracle_rows(blocks, x, rows)
+        assert_close(y.float().cpu().double().numpy()[rows], want, scale, c["out"], f"{name}[{i}] {m}x{n}x{k}")
