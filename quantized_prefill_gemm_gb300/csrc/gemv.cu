@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, kQuant ? 2 : 1) q4k_gemv_kernel(cons
     for (int round = 0; round < rounds; ++round) {
         const int sb = part + round * kParts;
         const bool active = sb < ksb;
-        if (!active) {   // nothing to do this round but the two warp barriers
+        if (!active) {   // nothing to do in this pass but the two warp barriers
             __syncwarp();
             __syncwarp();
             continue;
