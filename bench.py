@@ -110,7 +110,7 @@ def gemm_launches(m, n, k, sms):
     the GEMM and, when the last wave of tiles is split along k, the fixup."""
     tiles = -(-m // 128) * (n // 128)
     rem = tiles % sms
-    split = rem > 0 and min(sms // rem, k // 256) >= 2 and k // 256 >= 4
+    split = rem > 0 and min(sms // rem, max(2, k // 512)) >= 2 and k // 256 >= 4
     return 3 if split else 2
 
 

@@ -227,13 +227,17 @@ q4k_status run_gemm(const void* packed_w, int64_t n, int64_t k, void* ws, size_t
     // sums whichever output the call asks for.  Tiles of fewer than four
     // super-blocks are not split: the fixup launch costs more than the
     // shorter units save (measured: 256 x 512 at 64 tokens, 18.0 -> 15.8 us).
+    // A part holds at least two super-blocks: one-super-block parts (the 8
+    // leftover tiles of 11008 x 4096 at 2048 tokens in 16 parts) measured
+    // slower than 8 parts of two, by their per-unit start and the fixup's
+    // reads (the 7B stack 38,983 -> 39,133 tok/s with two).
     p.split = 1;
     p.part_sb = p.ksb;
     p.full_tiles = p.num_tiles;
     const int sms = std::min<int>(dev->sm_count, static_cast<int>(kMaxSplitUnits));
     const int rem = p.num_tiles % sms;
     if (rem > 0) {
-        const int parts = std::min(sms / rem, p.ksb);
+        const int parts = std::min(sms / rem, std::max(2, p.ksb / 2));
         if (parts >= 2 && p.ksb >= 4) {
             p.part_sb = (p.ksb + parts - 1) / parts;
             p.split = (p.ksb + p.part_sb - 1) / p.part_sb;

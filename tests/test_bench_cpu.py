@@ -38,7 +38,7 @@ def test_step_footprint_qproj_and_ffn_configs():
 
 @pytest.mark.parametrize("m,n,k,want", [
     (2048, 4096, 4096, 3),     # 512 tiles: 3 waves + 56, split 2 ways -> quantizer, GEMM, fixup
-    (2048, 11008, 4096, 3),    # 1376 tiles: 9 waves + 8, split 16 ways
+    (2048, 11008, 4096, 3),    # 1376 tiles: 9 waves + 8, split 8 ways (parts of two super-blocks)
     (2048, 4096, 11008, 3),    # 512 tiles, split 2 ways (43 super-blocks)
     (512, 4096, 4096, 2),      # 128 tiles: one partial wave that cannot split (152 // 128 = 1)
     (2432, 4096, 4096, 2),     # 19 x 32 = 608 tiles: exactly 4 waves, nothing left over

@@ -170,8 +170,9 @@ def test_k_split_tail_and_workspace_reuse(q4k):
     """Tiles left over after the last full wave are split along k into parts of
     whole super-blocks; each part stores its partial tile in the workspace and
     a fixup kernel adds them in part order.  16 tiles with 8 super-blocks each
-    split 8 ways on a 152-SM part: every output against the oracle, three
-    calls on one workspace giving the same bits."""
+    split 4 ways (parts of at least two super-blocks) on a 152-SM part: every
+    output against the oracle, three calls on one workspace giving the same
+    bits."""
     m, n, k = 256, 1024, 2048
     blocks, x = make_case(n, k, m, "outlier", seed=91)
     packed = q4k.q4k_pack_weights(to_dev(blocks), n, k)
