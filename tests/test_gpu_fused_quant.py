@@ -129,3 +129,19 @@ def test_fused_full_size_configs_sampled(q4k, name):
         torch.cuda.synchronize()
         want, scale = oracle_rows(blocks, x, rows)
         assert_close(y.float().cpu().double().numpy()[rows], want, scale, c["out"], f"{name}[{i}] {m}x{n}x{k}")
+
+
+def test_fused_strided_activations(q4k):
+    """x as the first k columns of wider rows (ldx > k): the same bits as the
+    contiguous copy."""
+    from quantized_prefill_gemm_gb300 import inputs
+
+    m, n, k, ld = 300, 1024, 4096, 4160
+    x = inputs.activations_torch(m, k, seed=71, kind="outlier", device=DEV)
+    big = torch.full((m, ld), float("nan"), dtype=torch.float32, device=DEV)
+    big[:, :k] = x
+    packed = q4k.q4k_pack_weights(inputs.q4k_blocks_torch(n, k, seed=72, device=DEV), n, k)
+    y_strided = q4k.q4k_gemm_inkernel_quant(packed, n, k, big[:, :k], out_dtype="bf16")
+    y_dense = q4k.q4k_gemm_inkernel_quant(packed, n, k, x.contiguous(), out_dtype="bf16")
+    torch.cuda.synchronize()
+    assert torch.equal(y_strided.view(torch.int16), y_dense.view(torch.int16))
